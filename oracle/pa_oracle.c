@@ -1,0 +1,325 @@
+/*
+ * pa_oracle.c -- fp64 CPU oracle for attention over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY. The test suite, the smoke check and the
+ * benchmark's CPU-baseline leg are the only callers of this library. The
+ * product path (the CUDA library under paged_kv_decode_18_gb300/) never
+ * links, loads or calls it, and the two share no code, header, table or
+ * helper. Everything here is deliberately plain and slow: scalar loops, fp64
+ * arithmetic, no tiling, no fusion, no reordering beyond the definitions.
+ *
+ * What it computes, and where the definitions come from:
+ *
+ *   Cache write ("S06/S11" of the course README "Build an LLM Inference Engine
+ *   From Scratch", section "The code asserts its own claims"; and the
+ *   "KV Cache > The Idea" section of the LLM inference engine work-log,
+ *   shehab-ashraf.github.io/posts/llm-inference): every new token's K and V
+ *   rows are stored once, at the physical slot its block manager handed out.
+ *   A slot is phys_block * block_size + offset_in_block. Negative slot = skip.
+ *
+ *   Attention (same work-log section, "Decode: ... this single Q attends over
+ *   the whole history"; course README curriculum row "Memory & KV Cache":
+ *   PagedAttention, GQA): for sequence s, query token j and query head h,
+ *     K_s[p] = k_cache[block_tables[s][p / BS]][h / G][p % BS][:]  (V alike)
+ *     pos(j) = c_s - Lq_s + j        (the query's own position in the context)
+ *     z_p    = scale * <q[j,h], K_s[p]>   for 0 <= p <= pos(j) (causal), or
+ *              for 0 <= p < c_s (non-causal)
+ *     M = max z, L = sum exp(z - M), out = sum exp(z - M) V_s[p] / L,
+ *     lse = M + ln L.
+ *   This is the plain two-pass softmax attention over the gathered context.
+ *
+ *   Split-K merge (course README, "s12: online softmax is exact; paged and
+ *   split-K variants agree"): given P partial results (o_i, lse_i) over
+ *   disjoint key ranges, LSE = M + ln sum_i exp(lse_i - M) with M = max lse_i,
+ *   out = sum_i exp(lse_i - LSE) o_i. Partials with lse_i = -inf are empty.
+ *
+ *   Online softmax (course README, "S12 ... FlashAttention"; "online softmax is
+ *   exact"): a second, independent attention routine that streams the keys in
+ *   tiles with a running max and running sum. It exists only so the tests can
+ *   check it against the two-pass routine.
+ *
+ * Numbers: bf16 inputs are bit patterns (uint16). They are widened to fp64
+ * exactly (bf16 -> fp32 is a 16-bit shift; fp32 -> fp64 is exact).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_RANGE (-2)
+#define ORACLE_ERR_NOMEM (-3)
+
+/* bf16 bit pattern -> double, exactly. */
+static double bf16_bits_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int pa_oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache write: k_cache[slot / BS][h][slot % BS][:] = k[t][h][:] (V alike).  */
+/* Byte copy; tokens with a negative slot are skipped. A slot beyond the pool */
+/* is an error and nothing further is written.                               */
+/* ------------------------------------------------------------------------ */
+int pa_oracle_reshape_and_cache(const uint16_t *k, const uint16_t *v,
+                                const int64_t *slot_mapping, int64_t num_tokens,
+                                int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, uint16_t *k_cache,
+                                uint16_t *v_cache) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * (int64_t)block_size) return ORACLE_ERR_RANGE;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_dim; ++d) {
+                int64_t src = ((t * num_kv_heads) + h) * (int64_t)head_dim + d;
+                int64_t dst = (((block * num_kv_heads) + h) * (int64_t)block_size + offset) *
+                                  (int64_t)head_dim + d;
+                k_cache[dst] = k[src];
+                v_cache[dst] = v[src];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Two-pass softmax attention of one query over n dense fp64 keys/values.    */
+/* n == 0 gives out = 0 and lse = -inf (softmax over nothing).               */
+/* ------------------------------------------------------------------------ */
+static void attend_two_pass(const double *q, const double *K, const double *V, int64_t n,
+                            int D, double scale, double *z, double *out, double *lse) {
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    /* logits */
+    for (int64_t p = 0; p < n; ++p) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += q[d] * K[p * D + d];
+        z[p] = scale * dot;
+    }
+    /* pass 1: max */
+    double M = z[0];
+    for (int64_t p = 1; p < n; ++p)
+        if (z[p] > M) M = z[p];
+    /* pass 2: normaliser and weighted sum of V */
+    double L = 0.0;
+    for (int64_t p = 0; p < n; ++p) {
+        double w = exp(z[p] - M);
+        L += w;
+        for (int d = 0; d < D; ++d) out[d] += w * V[p * D + d];
+    }
+    for (int d = 0; d < D; ++d) out[d] /= L;
+    *lse = M + log(L);
+}
+
+/* Online softmax over the same inputs: keys streamed in tiles of `tile`,  */
+/* with a running max m, running sum l and a rescaled accumulator.         */
+static void attend_online(const double *q, const double *K, const double *V, int64_t n, int D,
+                          double scale, int64_t tile, double *acc, double *out, double *lse) {
+    double m = -INFINITY, l = 0.0;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+    for (int64_t t0 = 0; t0 < n; t0 += tile) {
+        int64_t t1 = t0 + tile < n ? t0 + tile : n;
+        double tile_max = -INFINITY;
+        for (int64_t p = t0; p < t1; ++p) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += q[d] * K[p * D + d];
+            double s = scale * dot;
+            if (s > tile_max) tile_max = s;
+        }
+        double m_new = m > tile_max ? m : tile_max;
+        double alpha = exp(m - m_new); /* m = -inf on the first tile: alpha = 0 */
+        l *= alpha;
+        for (int d = 0; d < D; ++d) acc[d] *= alpha;
+        for (int64_t p = t0; p < t1; ++p) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += q[d] * K[p * D + d];
+            double w = exp(scale * dot - m_new);
+            l += w;
+            for (int d = 0; d < D; ++d) acc[d] += w * V[p * D + d];
+        }
+        m = m_new;
+    }
+    if (n == 0) {
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    for (int d = 0; d < D; ++d) out[d] = acc[d] / l;
+    *lse = m + log(l);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dense attention over contiguous bf16 keys/values, one query vector.       */
+/*   q: [D] bf16, K/V: [n, D] bf16 rows (row stride D).                      */
+/*   mode 0 = two-pass, mode 1 = online with the given tile.                 */
+/* ------------------------------------------------------------------------ */
+int pa_oracle_attention_dense(const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                              int64_t n, int D, double scale, int mode, int64_t tile,
+                              double *out, double *lse) {
+    if (n < 0 || D <= 0 || (mode == 1 && tile <= 0)) return ORACLE_ERR_ARG;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+    double *Kd = (double *)malloc(sizeof(double) * (size_t)(n * D + 1));
+    double *Vd = (double *)malloc(sizeof(double) * (size_t)(n * D + 1));
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)(n > D ? n + 1 : D + 1));
+    if (!qd || !Kd || !Vd || !tmp) {
+        free(qd); free(Kd); free(Vd); free(tmp);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int d = 0; d < D; ++d) qd[d] = bf16_bits_to_double(q[d]);
+    for (int64_t i = 0; i < n * D; ++i) {
+        Kd[i] = bf16_bits_to_double(K[i]);
+        Vd[i] = bf16_bits_to_double(V[i]);
+    }
+    if (mode == 0)
+        attend_two_pass(qd, Kd, Vd, n, D, scale, tmp, out, lse);
+    else
+        attend_online(qd, Kd, Vd, n, D, scale, tile, tmp, out, lse);
+    free(qd); free(Kd); free(Vd); free(tmp);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged attention. Shapes:                                                  */
+/*   q            [Tq, Hq, D] bf16, Tq = cu_seqlens_q[S]                     */
+/*   k/v_cache    [num_blocks, Hkv, BS, D] bf16                              */
+/*   block_tables [S, max_blocks] int32                                      */
+/*   context_lens [S] int32 (includes the sequence's own query tokens)       */
+/*   cu_seqlens_q [S + 1] int32 (row offsets of each sequence's queries)     */
+/*   out          [Tq, Hq, D] fp64;  lse [Tq, Hq] fp64 (natural log)         */
+/* Query head h reads KV head h / (Hq / Hkv).                                */
+/* mode 0 = two-pass (the oracle proper); mode 1 = online with `tile` keys.  */
+/* ------------------------------------------------------------------------ */
+int pa_oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *block_tables,
+                              const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                              double scale, int causal, int mode, int64_t tile,
+                              int num_threads, double *out, double *lse) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks_per_seq < 0 || num_q_heads % num_kv_heads != 0 ||
+        (mode == 1 && tile <= 0))
+        return ORACLE_ERR_ARG;
+    const int G = num_q_heads / num_kv_heads;
+    const int D = head_dim;
+    /* argument checks first, so the parallel loop cannot fail half way */
+    for (int s = 0; s < num_seqs; ++s) {
+        int c = context_lens[s];
+        int lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
+        if (c < 0 || lq < 0 || lq > c || c > max_blocks_per_seq * block_size)
+            return ORACLE_ERR_RANGE;
+        int nb = (c + block_size - 1) / block_size;
+        for (int b = 0; b < nb; ++b) {
+            int32_t phys = block_tables[(int64_t)s * max_blocks_per_seq + b];
+            if (phys < 0 || phys >= num_blocks) return ORACLE_ERR_RANGE;
+        }
+    }
+    const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int64_t pr = 0; pr < pairs; ++pr) {
+        const int s = (int)(pr / num_kv_heads);
+        const int kvh = (int)(pr % num_kv_heads);
+        const int64_t c = context_lens[s];
+        const int64_t q0 = cu_seqlens_q[s];
+        const int64_t lq = cu_seqlens_q[s + 1] - q0;
+        if (lq == 0) continue;
+        double *K = (double *)malloc(sizeof(double) * (size_t)(c * D + 1));
+        double *V = (double *)malloc(sizeof(double) * (size_t)(c * D + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)(c > D ? c + 1 : D + 1));
+        if (!K || !V || !qd || !tmp) {
+            free(K); free(V); free(qd); free(tmp);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+            continue;
+        }
+        /* gather this sequence's context for KV head kvh, in position order */
+        for (int64_t p = 0; p < c; ++p) {
+            int64_t phys = block_tables[(int64_t)s * max_blocks_per_seq + p / block_size];
+            int64_t row = ((phys * num_kv_heads + kvh) * block_size + p % block_size) * D;
+            for (int d = 0; d < D; ++d) {
+                K[p * D + d] = bf16_bits_to_double(k_cache[row + d]);
+                V[p * D + d] = bf16_bits_to_double(v_cache[row + d]);
+            }
+        }
+        for (int g = 0; g < G; ++g) {
+            const int h = kvh * G + g;
+            for (int64_t j = 0; j < lq; ++j) {
+                const int64_t row = q0 + j;
+                const int64_t pos = c - lq + j;          /* this query's position */
+                const int64_t n = causal ? pos + 1 : c;  /* keys it may see */
+                for (int d = 0; d < D; ++d)
+                    qd[d] = bf16_bits_to_double(q[(row * num_q_heads + h) * (int64_t)D + d]);
+                double *o = out + (row * num_q_heads + h) * (int64_t)D;
+                double *l = lse + row * num_q_heads + h;
+                if (mode == 0)
+                    attend_two_pass(qd, K, V, n, D, scale, tmp, o, l);
+                else
+                    attend_online(qd, K, V, n, D, scale, tile, tmp, o, l);
+            }
+        }
+        free(K); free(V); free(qd); free(tmp);
+    }
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Split-K merge of P partials per row.                                      */
+/*   part_out [rows, P, D] fp64, part_lse [rows, P] fp64 -> out [rows, D],   */
+/*   lse [rows]. Rows whose partials are all empty give 0 and -inf.          */
+/* ------------------------------------------------------------------------ */
+int pa_oracle_splitk_merge(const double *part_out, const double *part_lse, int64_t rows,
+                           int P, int D, double *out, double *lse) {
+    if (rows < 0 || P <= 0 || D <= 0) return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *li = part_lse + r * P;
+        double M = -INFINITY;
+        for (int i = 0; i < P; ++i)
+            if (li[i] > M) M = li[i];
+        double *o = out + r * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (M == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int i = 0; i < P; ++i) sum += exp(li[i] - M);
+        const double LSE = M + log(sum);
+        for (int i = 0; i < P; ++i) {
+            double w = exp(li[i] - LSE);
+            const double *oi = part_out + (r * P + i) * (int64_t)D;
+            for (int d = 0; d < D; ++d) o[d] += w * oi[d];
+        }
+        lse[r] = LSE;
+    }
+    return ORACLE_OK;
+}
