@@ -1,0 +1,218 @@
+/*
+ * pa.h -- C ABI of libpagedattn: attention over a paged KV cache on GB300
+ * (sm_103a).
+ *
+ * The operations follow the pages this library is built from:
+ *   - "KV Cache > The Idea" on the LLM inference engine work-log
+ *     (shehab-ashraf.github.io/posts/llm-inference): each step appends the new
+ *     tokens' K and V to the cache, then the new queries attend over the whole
+ *     history;
+ *   - "S20 - The Complete Engine", section "Core idea" (the engine's step()
+ *     loop): each request's block_table maps its logical blocks to physical
+ *     blocks that the block manager allocated;
+ *   - the course README "Build an LLM Inference Engine From Scratch",
+ *     curriculum rows "Memory & KV Cache" (PagedAttention, GQA) and
+ *     "Batching & Scheduling" (chunked prefill, FlashAttention), and the
+ *     claims "online softmax is exact; paged and split-K variants agree",
+ *     "chunked prefill produces a bit-identical KV cache".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *   - Pointers are DEVICE pointers unless stated otherwise. The caller owns
+ *     and allocates every buffer, including the workspace. The library
+ *     allocates no memory and never synchronises the stream on these calls.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t passed
+ *     as void*; NULL = the legacy default stream) of the CURRENT device.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (pa_bf16 = uint16_t).
+ *   - KV cache layout: k_cache and v_cache are separate arrays, each
+ *     [num_blocks][num_kv_heads][block_size][head_dim], contiguous. The
+ *     (block, kv head) tile of one block is block_size*head_dim contiguous
+ *     elements (4 KB at block_size 16, head_dim 128).
+ *   - A slot is phys_block * block_size + offset_in_block.
+ *   - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - context_lens[s] counts every token of sequence s that its queries may
+ *     see, INCLUDING the step's own new tokens (written first by
+ *     pa_reshape_and_cache). Query j of a sequence with q_len Lq sits at
+ *     position context_len - Lq + j.
+ *   - lse is the natural-log log-sum-exp of the scaled logits
+ *     (scale * q.k) over the keys a query sees, fp32, one per (query, head).
+ *   - Return value: PA_OK (0) or a negative pa_status. Host-side argument
+ *     checks run before anything is enqueued; a failing call enqueues nothing.
+ *     Values that live in device memory (slots, block ids, lengths) are
+ *     range-checked by the kernels: an out-of-range value sets a bit of the
+ *     device error word (read it with pa_debug_read_error) and the offending
+ *     access is skipped or clamped, never performed -- the kernels do not
+ *     trap. Results for the affected rows are then undefined.
+ *
+ * Built configuration: head_dim 128, block_size 16, and num_q_heads /
+ * num_kv_heads = 2 for pa_decode (1..8 for pa_decode_varlen with
+ * q tiles of 16 / group rows). Other shapes return PA_ERR_UNSUPPORTED.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pa_bf16;
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_ARG = -1,         /* null pointer, negative size, inconsistent shape */
+  PA_ERR_UNSUPPORTED = -2, /* shape not built (head_dim, block_size, group) */
+  PA_ERR_WORKSPACE = -3,   /* workspace missing, misaligned or too small */
+  PA_ERR_CUDA = -4,        /* a CUDA runtime call (launch, attribute query) failed */
+  PA_ERR_DEVICE = -5       /* device-side check failed (see pa_debug_read_error) */
+} pa_status;
+
+/* Bits of the device error word (pa_debug_read_error). */
+#define PA_DEVERR_SLOT_RANGE 0x1u    /* slot_mapping[t] >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_RANGE 0x2u   /* a used block_tables entry outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_RANGE 0x4u /* context_len < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEVERR_QLEN_RANGE 0x8u    /* q_len < 0, q_len > context_len, or cu_seqlens_q inconsistent */
+#define PA_DEVERR_PIPE_TIMEOUT 0x10u /* an asynchronous copy did not land within its time limit */
+#define PA_DEVERR_PLAN_OVERFLOW 0x20u /* work list larger than the launch was sized for */
+
+/* Problem shape, passed by pointer (host memory) to every call. */
+typedef struct pa_shape {
+  int num_seqs;           /* S: sequences in the batch */
+  int num_q_heads;        /* Hq */
+  int num_kv_heads;       /* Hkv; Hq % Hkv == 0 */
+  int head_dim;           /* D (built: 128) */
+  int block_size;         /* BS, tokens per physical block (built: 16) */
+  int max_blocks_per_seq; /* row length of block_tables */
+  int64_t num_blocks;     /* physical blocks in each of k_cache / v_cache */
+} pa_shape;
+
+/*
+ * pa_reshape_and_cache -- slot-mapped write of the step's new K/V rows into
+ * the block pool ("KV Cache > The Idea": the new K and V are appended to the
+ * cache; the course README's chunked-prefill claim: writing in chunks gives a
+ * bit-identical cache).
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim] bf16, contiguous
+ *   slot_mapping  [num_tokens] int64; slot < 0 means "skip this token"
+ *   k_cache, v_cache  the pool, layout above; written in place
+ *   shape         uses num_kv_heads, head_dim, block_size, num_blocks
+ *
+ * For every t with slot_mapping[t] >= 0 it copies the bytes of k[t][h][:]
+ * to k_cache[slot / BS][h][slot % BS][:] (V alike). A pure byte copy: the
+ * result is bit-exact. Two tokens with the same slot in one call race
+ * (undefined which one lands). A slot >= num_blocks*block_size is skipped
+ * and sets PA_DEVERR_SLOT_RANGE. num_tokens == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v, const int64_t* slot_mapping,
+                         int64_t num_tokens, pa_bf16* k_cache, pa_bf16* v_cache,
+                         const pa_shape* shape, void* stream);
+
+/*
+ * pa_decode -- one query token per sequence (q_len 1) attending over its
+ * paged context: block-table gather, GQA sharing of each K/V tile by the
+ * group's query heads, online softmax, and split-K over long contexts with a
+ * log-sum-exp merge ("online softmax is exact; paged and split-K variants
+ * agree").
+ *
+ *   q             [S][Hq][D] bf16
+ *   k_cache, v_cache  pool (read only)
+ *   block_tables  [S][max_blocks_per_seq] int32; entries past a sequence's
+ *                 ceil(context_len / BS) blocks are never read
+ *   context_lens  [S] int32, 0 <= c <= max_blocks_per_seq * BS. c == 0 gives
+ *                 out = 0 and lse = -inf for that sequence.
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(D))
+ *   out           [S][Hq][D] bf16 (round to nearest even from fp32)
+ *   lse           [S][Hq] fp32, natural log; may be NULL if not wanted
+ *   num_splits    0  = balanced: the library cuts the batch's total K/V tile
+ *                      count into equal contiguous ranges, one per resident
+ *                      warp, and merges the pieces of sequences that were cut;
+ *                 1  = no split: one warp per (sequence, KV head);
+ *                 P >= 2 = every (sequence, KV head) is cut into P near-equal
+ *                      block ranges whose partials are merged by
+ *                      pa_splitk_reduce (P <= 1024).
+ *   workspace     device scratch of at least pa_decode_workspace_size(...)
+ *                 bytes, 256-byte aligned; may be NULL when that size is 0.
+ *                 Its contents need no initialisation and are clobbered.
+ */
+int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace pa_decode needs for this shape and num_splits on the
+ * current device (0 when num_splits == 1). */
+size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits);
+
+/*
+ * pa_decode_varlen -- several query tokens per sequence over the same paged
+ * pool: speculative-decoding verify (1 + k draft tokens, causal within the
+ * query window; "S20 - The Complete Engine", step 3 PROPOSE and step 5
+ * verify) and chunked prefill (a chunk of queries at an offset whose earlier
+ * tokens are already cached; course README, "chunked prefill"). QK^T and PV
+ * run on the tensor cores in tiles of 16 rows = (16 / G) query tokens x G
+ * query heads of one KV head.
+ *
+ *   q             [num_q_tokens][Hq][D] bf16; sequence s owns rows
+ *                 cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1
+ *   cu_seqlens_q  [S+1] int32, cu_seqlens_q[0] == 0,
+ *                 cu_seqlens_q[S] == num_q_tokens, non-decreasing
+ *   max_q_len     an upper bound of the q_lens (host value, sizes the launch)
+ *   causal        1: query j sees keys 0 .. c - Lq + j; 0: it sees 0 .. c - 1
+ *   out, lse      [num_q_tokens][Hq][D] bf16, [num_q_tokens][Hq] fp32 (lse may
+ *                 be NULL)
+ *   workspace     at least pa_decode_varlen_workspace_size(...) bytes,
+ *                 256-byte aligned; clobbered.
+ * Work is balanced like pa_decode with num_splits == 0. A sequence with
+ * q_len 0 produces no rows.
+ */
+int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     const int32_t* cu_seqlens_q, int64_t num_q_tokens, int max_q_len,
+                     int causal, float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+size_t pa_decode_varlen_workspace_size(const pa_shape* shape, int64_t num_q_tokens,
+                                       int max_q_len);
+
+/*
+ * pa_splitk_reduce -- merge of split-K partial softmax results (course
+ * README, "online softmax is exact; paged and split-K variants agree").
+ * For each (row, head):
+ *   M = max_i lse_i,  LSE = M + ln sum_i exp(lse_i - M),
+ *   out = sum_i exp(lse_i - LSE) * o_i,  lse_out = LSE.
+ * Partials with lse_i = -inf are empty and weigh 0; a row whose partials are
+ * all empty gives out = 0 and lse_out = -inf.
+ *
+ *   part_out  [num_rows][num_heads][num_splits][head_dim] fp32 (each o_i is
+ *             already normalised by its own softmax sum)
+ *   part_lse  [num_rows][num_heads][num_splits] fp32, natural log
+ *   out       [num_rows][num_heads][head_dim] bf16
+ *   lse       [num_rows][num_heads] fp32, may be NULL
+ * head_dim must be a multiple of 4 and at most 1024; num_splits >= 1.
+ */
+int pa_splitk_reduce(const float* part_out, const float* part_lse, int64_t num_rows,
+                     int num_heads, int num_splits, int head_dim, pa_bf16* out, float* lse,
+                     void* stream);
+
+/* Text for a pa_status value (static storage). */
+const char* pa_status_string(int status);
+
+/*
+ * pa_debug_read_error -- synchronises `stream`, returns the device error word
+ * (an OR of PA_DEVERR_* bits, 0 if nothing was flagged) accumulated by every
+ * kernel of this library on the current device since the last read, and
+ * clears it. Returns PA_ERR_CUDA (negative) if the synchronisation or the
+ * copy fails. Not for the hot path: it blocks the host.
+ */
+int pa_debug_read_error(void* stream);
+
+/* Library version string, e.g. "pagedattn 0.1 sm_103a". */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,79 @@
+// pa_cache.cu -- slot-mapped write of the step's new K/V rows into the paged
+// pool (LLM inference engine work-log, "KV Cache > The Idea": the new K and V
+// are appended to the cache before the new queries attend; course README
+// "Build an LLM Inference Engine From Scratch": chunked prefill gives a
+// bit-identical cache).
+//
+// A byte copy: each thread moves one 16-byte chunk of K and the matching
+// chunk of V. Reads of k/v are fully coalesced; each (token, KV head) row
+// lands as one contiguous 256-byte run of the (block, KV head) tile.
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+constexpr int kChunksPerRow = kHeadDim * 2 / 16;  // 16-byte chunks per (token, head) row
+
+__global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                         const int64_t* __restrict__ slots, int64_t total_chunks,
+                                         int Hkv, int64_t num_slots, uint4* __restrict__ k_cache,
+                                         uint4* __restrict__ v_cache) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total_chunks) return;
+  const int per_token = Hkv * kChunksPerRow;
+  const int64_t t = i / per_token;
+  const int r = (int)(i - t * per_token);
+  const int h = r / kChunksPerRow, c = r % kChunksPerRow;
+  const int64_t slot = slots[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (r == 0) flag_error(PA_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const int64_t blk = slot / kBlock, off = slot % kBlock;
+  const int64_t dst = (((blk * Hkv + h) * kBlock + off) * kChunksPerRow) + c;
+  k_cache[dst] = k[i];
+  v_cache[dst] = v[i];
+}
+
+}  // namespace
+
+unsigned take_error_word_cache(cudaStream_t stream, int* rc) {
+  unsigned v = 0, zero = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&v, g_pa_error_word, sizeof v) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_pa_error_word, &zero, sizeof zero) != cudaSuccess) {
+    *rc = PA_ERR_CUDA;
+    return 0;
+  }
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v,
+                                    const int64_t* slot_mapping, int64_t num_tokens,
+                                    pa_bf16* k_cache, pa_bf16* v_cache, const pa_shape* shape,
+                                    void* stream) {
+  int rc = check_shape_common(shape);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_ARG;
+  const int64_t total = num_tokens * shape->num_kv_heads * kChunksPerRow;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 0x7fffffff) return PA_ERR_ARG;
+  reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), slot_mapping, total,
+      shape->num_kv_heads, shape->num_blocks * shape->block_size,
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache));
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}

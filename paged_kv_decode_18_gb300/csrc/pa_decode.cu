@@ -1,0 +1,694 @@
+// pa_decode.cu -- paged decode attention (one query token per sequence) on
+// the CUDA cores, the split-K partial merge, and their C-ABI entry points.
+//
+// What is computed (LLM inference engine work-log, "KV Cache > The Idea";
+// course README "Build an LLM Inference Engine From Scratch", curriculum row
+// "Memory & KV Cache" and the claim "online softmax is exact; paged and
+// split-K variants agree"): for every sequence s and query head h,
+//   out[s,h] = sum_p softmax_p(scale * q[s,h] . K_s[p]) V_s[p],
+//   lse[s,h] = ln sum_p exp(scale * q[s,h] . K_s[p]),
+// with K_s/V_s reached through the block table and KV head h / 2.
+//
+// Design (GB300): decode at q_len 1 is an HBM stream -- each K/V element read
+// feeds 2 query heads, about 2 flop/byte -- so it runs on the CUDA cores and
+// everything is arranged around moving bytes:
+//   * one warp is one worker; it owns a contiguous range of (sequence,
+//     KV head, block) tiles and a private ring of NSTAGE shared-memory stages;
+//   * lane 0 moves each 4 KB K tile and 4 KB V tile of one (block, KV head)
+//     with a 1-D bulk async copy (TMA engine) onto the stage's mbarrier, plus
+//     the 512 B of the two query heads when a new sequence starts;
+//   * both query heads of the KV head share every tile read from shared memory;
+//   * QK^T: lane (c, half) holds dims 8c..8c+7 for 8 tokens and both heads;
+//     the 16 partial dots are reduce-scattered over 16 lanes (15 shuffles)
+//     so each lane ends with one (token, head) score;
+//   * online softmax in the log2 domain (scale * log2 e folded into q);
+//   * PV: the same lane layout accumulates 2 heads x 8 dims in fp32.
+// A batch is cut into equal tile ranges over all resident warps (num_splits
+// 0), so ragged batches and long contexts balance; a (sequence, KV head) cut
+// by a range boundary leaves partials that a small merge kernel combines.
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+constexpr int kG = 2;                          // query heads per KV head (built)
+constexpr int kQBytes = kG * kHeadDim * 2;     // 512
+constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
+constexpr int kDescInts = 8;
+
+template <int NSTAGE>
+struct WarpLayout {
+  static constexpr int kBarOff = NSTAGE * kStageBytes;
+  static constexpr int kPOff = kBarOff + ((NSTAGE * 8 + 15) / 16) * 16;
+  static constexpr int kBytes = ((kPOff + 128 + 127) / 128) * 128;
+};
+
+enum : int { kBalanced = 0, kFixed = 1 };
+
+struct DecodeArgs {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  uint16_t* out;
+  float* lse;
+  float scale_log2;
+  int S, Hq, Hkv, max_blocks;
+  int64_t num_blocks;
+  int mode;         // kBalanced or kFixed
+  int num_splits;   // kFixed: P
+  int num_workers;  // kBalanced: warps launched
+  float* part_o;    // kBalanced: [NW*2][G][D]; kFixed: [S][Hq][P][D]
+  float* part_lse;  // kBalanced: [NW*2][G];    kFixed: [S][Hq][P]
+  int* desc;        // kBalanced: [NW][kDescInts]
+};
+
+__device__ __forceinline__ void unpack8(const uint4 w, float (&f)[8]) {
+  f[0] = bf_lo(w.x); f[1] = bf_hi(w.x); f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
+  f[4] = bf_lo(w.z); f[5] = bf_hi(w.z); f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
+}
+
+// Write 8 dims (one lane's chunk) of one output row as bf16.
+__device__ __forceinline__ void store_out8(uint16_t* dst, const float (&v)[8], float inv) {
+  uint4 o;
+  o.x = pack_bf2(v[0] * inv, v[1] * inv);
+  o.y = pack_bf2(v[2] * inv, v[3] * inv);
+  o.z = pack_bf2(v[4] * inv, v[5] * inv);
+  o.w = pack_bf2(v[6] * inv, v[7] * inv);
+  *reinterpret_cast<uint4*>(dst) = o;
+}
+
+__device__ __forceinline__ void store_f8(float* dst, const float (&v)[8], float inv) {
+  reinterpret_cast<float4*>(dst)[0] = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+}
+
+template <int NWARPS, int NSTAGE>
+__global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeArgs a) {
+  using L = WarpLayout<NSTAGE>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* wbuf = smem + warp * L::kBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + L::kBarOff);
+  float* pbuf = reinterpret_cast<float*>(wbuf + L::kPOff);
+  const int S = a.S, Hkv = a.Hkv, Hq = a.Hq;
+
+  int* pm = reinterpret_cast<int*>(smem + NWARPS * L::kBytes);
+  PlanSmem P;
+  P.pair_off = pm;
+  P.seq_pair = P.pair_off + (S + 1);
+  P.ctx = P.seq_pair + (S + 1);
+  P.qstart = P.ctx + S;
+  int* scratch = P.qstart + (S + 1);
+
+  if (lane == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    mbar_fence_init();
+  }
+  PlanInputs in;
+  in.context_lens = a.context_lens;
+  in.cu_seqlens_q = nullptr;
+  in.S = S;
+  in.Hkv = Hkv;
+  in.max_ctx = a.max_blocks * kBlock;
+  in.qtile = 1;
+  in.causal = 1;
+  in.npairs_cap = S;
+  in.num_q_rows = S;
+  build_plan(in, P, scratch);  // ends with __syncthreads: barrier inits visible too
+
+  const int W = P.total;
+  const int w = blockIdx.x * NWARPS + warp;
+
+  // Sequences with an empty context: out = 0, lse = -inf (balanced mode owns
+  // them in CTA 0; fixed mode handles them through its empty partials).
+  if (a.mode == kBalanced && blockIdx.x == 0) {
+    for (int s = warp; s < S; s += NWARPS) {
+      if (P.ctx[s] != 0) continue;
+      for (int h = 0; h < Hq; ++h) {
+        uint2 z = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(a.out + ((size_t)s * Hq + h) * kHeadDim + lane * 4) = z;
+        if (a.lse && lane == 0) a.lse[(size_t)s * Hq + h] = neg_inf();
+      }
+    }
+  }
+
+  int R0 = 0, R1 = 0, fixed_p = 0;
+  if (a.mode == kBalanced) {
+    const int nw = min(a.num_workers, W);
+    if (w < nw) {
+      R0 = (int)((int64_t)w * W / nw);
+      R1 = (int)((int64_t)(w + 1) * W / nw);
+    }
+    if (w < a.num_workers && lane == 0) {
+      // Does this worker own the merge of the segment its range starts in?
+      int d[5] = {-1, 0, 0, 0, 0};
+      if (R0 < R1) {
+        const TilePos t = locate(P, S, Hkv, R0);
+        const int A = R0 - t.b;  // flat start of the segment
+        const int R0prev = w > 0 ? (int)((int64_t)(w - 1) * W / nw) : 0;
+        if (t.b > 0 && A >= R0prev) {
+          const int B = A + t.nt;
+          d[0] = t.s;
+          d[1] = t.h;
+          d[2] = (int)(((int64_t)B * nw - 1) / W);  // worker holding the last tile
+          d[3] = (A == R0prev) ? 0 : 1;              // slot of worker w-1's piece
+        }
+      }
+      int* dd = a.desc + (size_t)w * kDescInts;
+      for (int i = 0; i < 5; ++i) dd[i] = d[i];
+    }
+  } else {
+    const int PS = a.num_splits;
+    if ((int64_t)w >= (int64_t)S * Hkv * PS) return;
+    const int s = w / (Hkv * PS), h = (w / PS) % Hkv;
+    fixed_p = w % PS;
+    const int pr = P.seq_pair[s];
+    const bool has = P.seq_pair[s + 1] > pr;
+    const int nt = has ? (P.pair_off[pr + 1] - P.pair_off[pr]) / Hkv : 0;
+    const int b0 = (int)((int64_t)fixed_p * nt / PS), b1 = (int)((int64_t)(fixed_p + 1) * nt / PS);
+    if (b0 == b1) {
+      // empty piece: P == 1 -> the row itself (0, -inf); else an empty partial
+      for (int g = 0; g < kG; ++g) {
+        const size_t row = (size_t)s * Hq + h * kG + g;
+        if (PS == 1) {
+          *reinterpret_cast<uint2*>(a.out + row * kHeadDim + lane * 4) = make_uint2(0u, 0u);
+          if (a.lse && lane == 0) a.lse[row] = neg_inf();
+        } else {
+          *reinterpret_cast<float4*>(a.part_o + (row * PS + fixed_p) * kHeadDim + lane * 4) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane == 0) a.part_lse[row * PS + fixed_p] = neg_inf();
+        }
+      }
+      return;
+    }
+    R0 = P.pair_off[pr] + h * nt + b0;
+    R1 = R0 + (b1 - b0);
+  }
+  if (R0 >= R1) return;
+
+  const int c16 = lane & 15;  // dims 8*c16 .. 8*c16+7
+  const int th = lane >> 4;   // tokens 8*th .. 8*th+7 of a tile
+  const int hsel = lane & 1;  // head of the score this lane ends up holding
+
+  // ---- producer state -----------------------------------------------------
+  TilePos pp = locate(P, S, Hkv, R0);
+  int pidx = R0;
+  int wbase = R0;
+  auto load_phys = [&](int idx) -> int {
+    if (idx >= R1) return 0;
+    const TilePos t = locate(P, S, Hkv, idx);
+    return a.block_tables[(size_t)t.s * a.max_blocks + t.b];
+  };
+  int phys_cur = load_phys(wbase + lane);
+  int phys_next = load_phys(wbase + 32 + lane);
+
+  auto issue = [&](int stage) {
+    int phys = __shfl_sync(kFull, phys_cur, pidx - wbase);
+    const bool first = (pidx == R0) || (pp.b == 0);
+    if (lane == 0) {
+      if (phys < 0 || (int64_t)phys >= a.num_blocks) {
+        flag_error(PA_DEVERR_BLOCK_RANGE);
+        phys = 0;
+      }
+      unsigned char* st = wbuf + stage * kStageBytes;
+      const uint32_t bar = smem_addr(&bars[stage]);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, 2 * kTileBytes + (first ? kQBytes : 0));
+      const size_t tile = ((size_t)phys * Hkv + pp.h) * (kBlock * kHeadDim);
+      bulk_copy_g2s(smem_addr(st), a.k_cache + tile, kTileBytes, bar);
+      bulk_copy_g2s(smem_addr(st + kTileBytes), a.v_cache + tile, kTileBytes, bar);
+      if (first)
+        bulk_copy_g2s(smem_addr(st + 2 * kTileBytes),
+                      a.q + ((size_t)pp.s * Hq + (size_t)pp.h * kG) * kHeadDim, kQBytes, bar);
+    }
+    ++pidx;
+    if (pidx < R1) advance(P, S, Hkv, pp);
+    if (pidx - wbase == 32) {
+      wbase += 32;
+      phys_cur = phys_next;
+      phys_next = load_phys(wbase + 32 + lane);
+    }
+  };
+
+  for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
+
+  // ---- consumer -------------------------------------------------------------
+  TilePos cp = locate(P, S, Hkv, R0);
+  float qf[kG][8];
+  float acc[kG][8];
+  float m0 = neg_inf(), m1 = neg_inf(), l_lane = 0.f;
+  int piece_b0 = 0;
+  bool piece_first = true;
+
+  int k = 0;
+  for (int idx = R0; idx < R1; ++idx, ++k) {
+    const int stage = k % NSTAGE;
+    const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
+    if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
+      // a copy never landed: give the remaining ones a bounded wait, then stop
+      for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
+        mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
+      return;
+    }
+    const unsigned char* st = wbuf + stage * kStageBytes;
+    const bool first = (idx == R0) || (cp.b == 0);
+    if (first) {
+      const uint4 q0 = *reinterpret_cast<const uint4*>(st + 2 * kTileBytes + c16 * 16);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(st + 2 * kTileBytes + 256 + c16 * 16);
+      unpack8(q0, qf[0]);
+      unpack8(q1, qf[1]);
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        qf[0][d] *= a.scale_log2;
+        qf[1][d] *= a.scale_log2;
+        acc[0][d] = 0.f;
+        acc[1][d] = 0.f;
+      }
+      m0 = neg_inf();
+      m1 = neg_inf();
+      l_lane = 0.f;
+      piece_b0 = cp.b;
+      piece_first = (idx == R0);
+    }
+    const int nvalid = min(kBlock, P.ctx[cp.s] - cp.b * kBlock);
+
+    // ---- scores: 8 tokens x 2 heads of partial dots per lane ---------------
+    float sc[16];
+    const unsigned char* Ks = st + th * 8 * 256 + c16 * 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 kw = *reinterpret_cast<const uint4*>(Ks + i * 256);
+      float kf[8];
+      unpack8(kw, kf);
+      float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        d0 = fmaf(qf[0][d], kf[d], d0);
+        d1 = fmaf(qf[1][d], kf[d], d1);
+      }
+      sc[2 * i] = d0;
+      sc[2 * i + 1] = d1;
+    }
+    // reduce-scatter over the 16 lanes of this half-warp: value v = 2*i + g
+    // ends in the lane with (lane & 15) == v
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+      const int half = 8 >> step;
+      const bool upper = (lane & half) != 0;
+#pragma unroll
+      for (int j = 0; j < half; ++j) {
+        const float send = upper ? sc[j] : sc[j + half];
+        const float keep = upper ? sc[j + half] : sc[j];
+        sc[j] = keep + __shfl_xor_sync(kFull, send, half);
+      }
+    }
+    const int tok = th * 8 + ((lane & 15) >> 1);
+    float s_val = tok < nvalid ? sc[0] : neg_inf();
+
+    // ---- online softmax (log2 domain) ------------------------------------------
+    float mx = s_val;
+#pragma unroll
+    for (int o = 2; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    const float mx_other = __shfl_xor_sync(kFull, mx, 1);
+    const float mn0 = fmaxf(m0, hsel ? mx_other : mx);
+    const float mn1 = fmaxf(m1, hsel ? mx : mx_other);
+    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const float p = ex2(s_val - (hsel ? mn1 : mn0));
+    l_lane = l_lane * (hsel ? al1 : al0) + p;
+    pbuf[lane] = p;  // index 2*token_in_half + head, halves at 0 and 16
+    __syncwarp();
+    float pv[16];
+    {
+      const float4* pb = reinterpret_cast<const float4*>(pbuf + th * 16);
+      const float4 p0 = pb[0], p1 = pb[1], p2 = pb[2], p3 = pb[3];
+      pv[0] = p0.x; pv[1] = p0.y; pv[2] = p0.z; pv[3] = p0.w;
+      pv[4] = p1.x; pv[5] = p1.y; pv[6] = p1.z; pv[7] = p1.w;
+      pv[8] = p2.x; pv[9] = p2.y; pv[10] = p2.z; pv[11] = p2.w;
+      pv[12] = p3.x; pv[13] = p3.y; pv[14] = p3.z; pv[15] = p3.w;
+    }
+    if (al0 != 1.f || al1 != 1.f) {
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        acc[0][d] *= al0;
+        acc[1][d] *= al1;
+      }
+    }
+    // ---- PV ----------------------------------------------------------------------
+    const unsigned char* Vs = st + kTileBytes + th * 8 * 256 + c16 * 16;
+    if (nvalid == kBlock) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 vw = *reinterpret_cast<const uint4*>(Vs + i * 256);
+        float vf[8];
+        unpack8(vw, vf);
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          acc[0][d] = fmaf(pv[2 * i], vf[d], acc[0][d]);
+          acc[1][d] = fmaf(pv[2 * i + 1], vf[d], acc[1][d]);
+        }
+      }
+    } else {
+      // tokens past the context may hold anything (even NaN): skip, never 0*x
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (th * 8 + i < nvalid) {
+          const uint4 vw = *reinterpret_cast<const uint4*>(Vs + i * 256);
+          float vf[8];
+          unpack8(vw, vf);
+#pragma unroll
+          for (int d = 0; d < 8; ++d) {
+            acc[0][d] = fmaf(pv[2 * i], vf[d], acc[0][d]);
+            acc[1][d] = fmaf(pv[2 * i + 1], vf[d], acc[1][d]);
+          }
+        }
+      }
+    }
+    __syncwarp();  // all lanes are done with this stage and with pbuf
+
+    if (pidx < R1) issue(stage);
+
+    const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
+    if (last) {
+      // ---- finish the piece -------------------------------------------------------
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        acc[0][d] += __shfl_xor_sync(kFull, acc[0][d], 16);
+        acc[1][d] += __shfl_xor_sync(kFull, acc[1][d], 16);
+      }
+      float ls = l_lane;
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) ls += __shfl_xor_sync(kFull, ls, o);
+      const float lo = __shfl_xor_sync(kFull, ls, 1);
+      const float l0 = hsel ? lo : ls, l1 = hsel ? ls : lo;
+      const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
+      const float lse0 = (m0 + lg2(l0)) * kLn2, lse1 = (m1 + lg2(l1)) * kLn2;
+      const size_t row0 = (size_t)cp.s * Hq + (size_t)cp.h * kG;
+      if (a.mode == kFixed && a.num_splits > 1) {
+        const int PS = a.num_splits;
+        if (th == 0) {
+          store_f8(a.part_o + ((row0 + 0) * PS + fixed_p) * kHeadDim + c16 * 8, acc[0], 1.f / l0);
+          store_f8(a.part_o + ((row0 + 1) * PS + fixed_p) * kHeadDim + c16 * 8, acc[1], 1.f / l1);
+        }
+        if (lane == 0) {
+          a.part_lse[(row0 + 0) * PS + fixed_p] = lse0;
+          a.part_lse[(row0 + 1) * PS + fixed_p] = lse1;
+        }
+      } else if (complete) {
+        if (th == 0) {
+          store_out8(a.out + (row0 + 0) * kHeadDim + c16 * 8, acc[0], 1.f / l0);
+          store_out8(a.out + (row0 + 1) * kHeadDim + c16 * 8, acc[1], 1.f / l1);
+        }
+        if (a.lse && lane == 0) {
+          a.lse[row0 + 0] = lse0;
+          a.lse[row0 + 1] = lse1;
+        }
+      } else {
+        const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
+        if (th == 0) {
+          store_f8(a.part_o + (slot * kG + 0) * kHeadDim + c16 * 8, acc[0], 1.f / l0);
+          store_f8(a.part_o + (slot * kG + 1) * kHeadDim + c16 * 8, acc[1], 1.f / l1);
+        }
+        if (lane == 0) {
+          a.part_lse[slot * kG + 0] = lse0;
+          a.part_lse[slot * kG + 1] = lse1;
+        }
+      }
+    }
+    if (idx + 1 < R1) advance(P, S, Hkv, cp);
+  }
+}
+
+// Merge the pieces of every (sequence, KV head) that the balanced ranges cut.
+// One warp per worker boundary; the owner recorded in desc[w] merges the
+// pieces held by workers w-1 .. last.
+__global__ void decode_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
+                                    const float* __restrict__ part_lse, int num_workers, int Hq,
+                                    uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= num_workers) return;
+  const int* d = desc + (size_t)w * kDescInts;
+  const int s = d[0];
+  if (s < 0) return;
+  const int h = d[1], last = d[2], slot_prev = d[3];
+  float mx[kG], sum[kG], LSE[kG];
+  for (int g = 0; g < kG; ++g) mx[g] = neg_inf();
+  for (int x = w - 1; x <= last; ++x) {
+    const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+    for (int g = 0; g < kG; ++g) mx[g] = fmaxf(mx[g], part_lse[slot * kG + g]);
+  }
+  for (int g = 0; g < kG; ++g) sum[g] = 0.f;
+  for (int x = w - 1; x <= last; ++x) {
+    const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+    for (int g = 0; g < kG; ++g) sum[g] += ex2((part_lse[slot * kG + g] - mx[g]) * kLog2e);
+  }
+  for (int g = 0; g < kG; ++g) LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
+  float4 acc[kG];
+  for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int x = w - 1; x <= last; ++x) {
+    const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+    for (int g = 0; g < kG; ++g) {
+      const float wt = ex2((part_lse[slot * kG + g] - LSE[g]) * kLog2e);
+      const float4 o =
+          *reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4);
+      acc[g].x = fmaf(wt, o.x, acc[g].x);
+      acc[g].y = fmaf(wt, o.y, acc[g].y);
+      acc[g].z = fmaf(wt, o.z, acc[g].z);
+      acc[g].w = fmaf(wt, o.w, acc[g].w);
+    }
+  }
+  for (int g = 0; g < kG; ++g) {
+    const size_t row = (size_t)s * Hq + (size_t)h * kG + g;
+    uint2 o;
+    o.x = pack_bf2(acc[g].x, acc[g].y);
+    o.y = pack_bf2(acc[g].z, acc[g].w);
+    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane * 4) = o;
+    if (lse && lane == 0) lse[row] = LSE[g];
+  }
+}
+
+// Split-K merge over a regular [rows][heads][P][D] partial layout: one warp
+// per (row, head).
+__global__ void splitk_reduce_kernel(const float* __restrict__ part_o,
+                                     const float* __restrict__ part_lse, int64_t nrh, int P,
+                                     int D, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int64_t rh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (rh >= nrh) return;
+  const float* L = part_lse + rh * P;
+  float mx = neg_inf();
+  for (int i = lane; i < P; i += 32) mx = fmaxf(mx, L[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  uint16_t* orow = out + rh * D;
+  if (mx == neg_inf()) {
+    for (int d = lane * 4; d < D; d += 128)
+      *reinterpret_cast<uint2*>(orow + d) = make_uint2(0u, 0u);
+    if (lse && lane == 0) lse[rh] = neg_inf();
+    return;
+  }
+  float sum = 0.f;
+  for (int i = lane; i < P; i += 32) sum += ex2((L[i] - mx) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+  const float LSE = mx + lg2(sum) * kLn2;
+  const float* O = part_o + rh * (int64_t)P * D;
+  for (int d = lane * 4; d < D; d += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < P; i0 += 32) {
+      const float wl = (i0 + lane < P) ? ex2((L[i0 + lane] - LSE) * kLog2e) : 0.f;
+      const int n = min(32, P - i0);
+      for (int j = 0; j < n; ++j) {
+        const float wt = __shfl_sync(kFull, wl, j);
+        const float4 o = *reinterpret_cast<const float4*>(O + (int64_t)(i0 + j) * D + d);
+        acc.x = fmaf(wt, o.x, acc.x);
+        acc.y = fmaf(wt, o.y, acc.y);
+        acc.z = fmaf(wt, o.z, acc.z);
+        acc.w = fmaf(wt, o.w, acc.w);
+      }
+    }
+    uint2 o;
+    o.x = pack_bf2(acc.x, acc.y);
+    o.y = pack_bf2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(orow + d) = o;
+  }
+  if (lse && lane == 0) lse[rh] = LSE;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+
+struct DecodeGeometry {
+  int mode = kBalanced;
+  int P = 0;
+  int grid = 0;
+  int workers = 0;
+  size_t smem = 0;
+  size_t ws_desc = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
+};
+
+inline size_t plan_smem_bytes(int S) { return sizeof(int) * (4 * (size_t)S + 3 + 40); }
+
+int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return PA_ERR_CUDA;
+  const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
+  g->smem = (size_t)kWarps * WarpLayout<kStages>::kBytes + plan_smem_bytes(S);
+  if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
+  auto kern = paged_decode_kernel<kWarps, kStages>;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)g->smem) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  if (num_splits == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, g->smem) !=
+            cudaSuccess ||
+        per_sm <= 0)
+      return PA_ERR_CUDA;
+    g->mode = kBalanced;
+    g->grid = dev.num_sms * per_sm;
+    g->workers = g->grid * kWarps;
+    g->ws_desc = round_up(sizeof(int) * kDescInts * (size_t)g->workers, 256);
+    g->ws_lse = round_up(sizeof(float) * 2 * kG * (size_t)g->workers, 256);
+    g->ws_o = round_up(sizeof(float) * 2 * kG * kHeadDim * (size_t)g->workers, 256);
+  } else {
+    g->mode = kFixed;
+    g->P = num_splits;
+    const int64_t warps = (int64_t)S * Hkv * num_splits;
+    if ((warps + kWarps - 1) / kWarps > 0x7fffffff) return PA_ERR_ARG;
+    g->grid = (int)((warps + kWarps - 1) / kWarps);
+    g->workers = (int)warps;
+    if (num_splits > 1) {
+      g->ws_lse = round_up(sizeof(float) * (size_t)S * Hq * num_splits, 256);
+      g->ws_o = round_up(sizeof(float) * (size_t)S * Hq * num_splits * kHeadDim, 256);
+    }
+  }
+  g->ws_bytes = g->ws_desc + g->ws_lse + g->ws_o;
+  return PA_OK;
+}
+
+int check_decode_args(const pa_shape* shape, int num_splits) {
+  int rc = check_shape_common(shape);
+  if (rc != PA_OK) return rc;
+  if (shape->num_q_heads != kG * shape->num_kv_heads) return PA_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > 1024) return PA_ERR_ARG;
+  if ((int64_t)shape->num_seqs * shape->num_kv_heads * (shape->max_blocks_per_seq + 1) >
+      0x3fffffff)
+    return PA_ERR_ARG;
+  return PA_OK;
+}
+
+}  // namespace
+
+unsigned take_error_word_decode(cudaStream_t stream, int* rc) {
+  unsigned v = 0, zero = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&v, g_pa_error_word, sizeof v) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_pa_error_word, &zero, sizeof zero) != cudaSuccess) {
+    *rc = PA_ERR_CUDA;
+    return 0;
+  }
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits) {
+  if (check_decode_args(shape, num_splits) != PA_OK) return 0;
+  if (shape->num_seqs == 0) return 0;
+  DecodeGeometry g;
+  if (decode_geometry(shape, num_splits, &g) != PA_OK) return 0;
+  return g.ws_bytes;
+}
+
+extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                         pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_decode_args(shape, num_splits);
+  if (rc != PA_OK) return rc;
+  if (shape->num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (lse && !aligned(lse, 4)))
+    return PA_ERR_ARG;
+  if (!(scale == scale)) return PA_ERR_ARG;
+  DecodeGeometry g;
+  rc = decode_geometry(shape, num_splits, &g);
+  if (rc != PA_OK) return rc;
+  if (g.ws_bytes > 0 &&
+      (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256)))
+    return PA_ERR_WORKSPACE;
+
+  DecodeArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.lse = lse;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.S = shape->num_seqs;
+  a.Hq = shape->num_q_heads;
+  a.Hkv = shape->num_kv_heads;
+  a.max_blocks = shape->max_blocks_per_seq;
+  a.num_blocks = shape->num_blocks;
+  a.mode = g.mode;
+  a.num_splits = g.P;
+  a.num_workers = g.workers;
+  char* ws = static_cast<char*>(workspace);
+  a.desc = g.ws_desc ? reinterpret_cast<int*>(ws) : nullptr;
+  a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
+  a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  paged_decode_kernel<kWarps, kStages><<<g.grid, kWarps * 32, g.smem, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (g.mode == kBalanced) {
+    const int wpb = 8;
+    decode_fixup_kernel<<<(g.workers + wpb - 1) / wpb, wpb * 32, 0, st>>>(
+        a.desc, a.part_o, a.part_lse, g.workers, a.Hq, out, lse);
+  } else if (g.P > 1) {
+    const int64_t nrh = (int64_t)a.S * a.Hq;
+    const int wpb = 8;
+    splitk_reduce_kernel<<<(unsigned)((nrh + wpb - 1) / wpb), wpb * 32, 0, st>>>(
+        a.part_o, a.part_lse, nrh, g.P, kHeadDim, out, lse);
+  }
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" int pa_splitk_reduce(const float* part_out, const float* part_lse, int64_t num_rows,
+                                int num_heads, int num_splits, int head_dim, pa_bf16* out,
+                                float* lse, void* stream) {
+  if (num_rows < 0 || num_heads <= 0 || num_splits <= 0 || head_dim <= 0) return PA_ERR_ARG;
+  if (head_dim % 4 != 0 || head_dim > 1024) return PA_ERR_UNSUPPORTED;
+  if (num_rows == 0) return PA_OK;
+  if (!part_out || !part_lse || !out) return PA_ERR_ARG;
+  if (!aligned(part_out, 16) || !aligned(part_lse, 4) || !aligned(out, 8) ||
+      (lse && !aligned(lse, 4)))
+    return PA_ERR_ARG;
+  const int64_t nrh = num_rows * num_heads;
+  const int wpb = 8;
+  const int64_t blocks = (nrh + wpb - 1) / wpb;
+  if (blocks > 0x7fffffff) return PA_ERR_ARG;
+  splitk_reduce_kernel<<<(unsigned)blocks, wpb * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      part_out, part_lse, nrh, num_splits, head_dim, out, lse);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}

@@ -1,0 +1,373 @@
+// pa_device.cuh -- device-side building blocks shared by the kernels of
+// libpagedattn (sm_103a): asynchronous-copy and mbarrier wrappers, the
+// tensor-core fragments, the device error word, and the per-CTA work plan
+// that cuts a batch of paged sequences into equal tile ranges.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kHeadDim = 128;                        // built head_dim
+constexpr int kBlock = 16;                           // built block_size (tokens)
+constexpr int kTileBytes = kBlock * kHeadDim * 2;    // one (block, kv head) K or V tile
+constexpr unsigned kFull = 0xffffffffu;
+
+// Time limit of every wait on an asynchronous copy. A copy that has not landed
+// by then sets PA_DEVERR_PIPE_TIMEOUT and the waiting warp gives up.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// device error word: one per translation unit (each TU owns its copy and
+// exposes a host reader), OR-ed together by pa_debug_read_error.
+// ---------------------------------------------------------------------------
+static __device__ unsigned int g_pa_error_word = 0;
+
+__device__ __forceinline__ void flag_error(unsigned bits) {
+  atomicOr(&g_pa_error_word, bits);
+}
+
+// ---------------------------------------------------------------------------
+// small PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier. Returns false (and flags
+// PA_DEVERR_PIPE_TIMEOUT) if the phase did not complete within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      flag_error(PA_DEVERR_PIPE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy / TMA) writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier.
+// dst/src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// 2-D tiled TMA load (tensor map in kernel parameter space) into shared
+// memory, completion counted on an mbarrier. x (innermost) in elements.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// fast exp2 / log2 (PTX approximate instructions; relative error ~2^-22)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// bf16 pair (one 32-bit word) -> two floats: low element, high element.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// float -> bf16 bits, round to nearest even (NaN kept NaN).
+__device__ __forceinline__ uint32_t f2bf_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  return f2bf_bits(lo) | (f2bf_bits(hi) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// tensor-core fragments (mma.sync m16n8k16, bf16 x bf16 -> fp32)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// Work plan.
+//
+// The batch is a list of (sequence, query tile) pairs; pair p needs n_p K/V
+// tiles (16 keys each) for each of the Hkv KV heads. Flat tile index order is
+// (pair, kv head, tile), so every (pair, kv head) -- a "segment" -- is a
+// contiguous run of n_p indices. pair_off[p] = Hkv * sum_{p' < p} n_p'. Each
+// CTA rebuilds this prefix in its shared memory from context_lens and
+// cu_seqlens_q (a few KB), so no separate planning kernel or host sync is
+// needed; warps then locate their ranges by binary search.
+// ---------------------------------------------------------------------------
+struct PlanSmem {
+  int* pair_off;   // [npairs_cap + 1]
+  int* seq_pair;   // [S + 1]  first pair of each sequence
+  int* ctx;        // [S]      context length (validated)
+  int* qstart;     // [S + 1]  cu_seqlens_q (validated)
+  int npairs;
+  int total;       // total flat tiles
+};
+
+struct PlanInputs {
+  const int32_t* context_lens;  // [S]
+  const int32_t* cu_seqlens_q;  // [S + 1] or nullptr (decode: one query per sequence)
+  int S;
+  int Hkv;
+  int max_ctx;       // max_blocks_per_seq * block size
+  int qtile;         // query tokens per tile (1 for decode)
+  int causal;
+  int npairs_cap;
+  int64_t num_q_rows;  // rows of q / out; every sequence's rows must lie inside
+};
+
+// Exclusive scan of n ints in shared memory, in place, by the whole CTA.
+// Returns the total. Uses `scratch` (>= 33 ints) for the warp partials.
+__device__ inline int block_exclusive_scan(int* data, int n, int* scratch) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int chunk = (n + nthreads - 1) / nthreads;
+  const int b = min(n, tid * chunk), e = min(n, b + chunk);
+  int local = 0;
+  for (int i = b; i < e; ++i) local += data[i];
+  // inclusive scan of `local` across the CTA
+  const int lane = tid & 31, warp = tid >> 5, nwarps = (nthreads + 31) >> 5;
+  int x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = lane < nwarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(kFull, wv, o);
+      if (lane >= o) wv += y;
+    }
+    if (lane < nwarps) scratch[lane] = wv;  // inclusive warp totals
+  }
+  __syncthreads();
+  int run = x - local + (warp > 0 ? scratch[warp - 1] : 0);  // exclusive start
+  for (int i = b; i < e; ++i) {
+    int v = data[i];
+    data[i] = run;
+    run += v;
+  }
+  const int total = scratch[nwarps - 1];
+  __syncthreads();
+  return total;
+}
+
+// Number of key tiles query tile qt of sequence s needs (per KV head).
+__device__ __forceinline__ int pair_tiles(int c, int lq, int qt, int qtile, int causal) {
+  int kv_end = causal ? (c - lq + min(qtile * (qt + 1), lq)) : c;
+  return (kv_end + kBlock - 1) / kBlock;
+}
+
+// Build the plan in shared memory. All threads of the CTA must call it.
+// Invalid lengths are clamped (and flagged) so that every later access stays
+// inside the caller's buffers.
+__device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* scratch) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int S = in.S;
+  for (int s = tid; s < S; s += nthreads) {
+    int c = in.context_lens[s];
+    if (c < 0 || c > in.max_ctx) {
+      flag_error(PA_DEVERR_CONTEXT_RANGE);
+      c = c < 0 ? 0 : in.max_ctx;
+    }
+    int lq = 1, q0 = s;
+    if (in.cu_seqlens_q) {
+      q0 = in.cu_seqlens_q[s];
+      lq = in.cu_seqlens_q[s + 1] - q0;
+      if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) {
+        flag_error(PA_DEVERR_QLEN_RANGE);
+        lq = 0;  // the sequence produces no rows
+      }
+    } else if (c == 0) {
+      lq = 0;  // decode with an empty context: written separately as 0 / -inf
+    }
+    P.ctx[s] = c;
+    P.qstart[s] = q0;
+    P.seq_pair[s] = (lq + in.qtile - 1) / in.qtile;  // query tiles of s
+    if (s == S - 1) P.qstart[S] = in.cu_seqlens_q ? in.cu_seqlens_q[S] : S;
+  }
+  __syncthreads();
+  int npairs = block_exclusive_scan(P.seq_pair, S, scratch);
+  if (tid == 0) P.seq_pair[S] = npairs;
+  if (npairs > in.npairs_cap) {
+    if (tid == 0) flag_error(PA_DEVERR_PLAN_OVERFLOW);
+    npairs = 0;  // do nothing rather than overflow the shared arrays
+  }
+  __syncthreads();
+  // tiles per pair (times Hkv)
+  for (int s = tid; s < S; s += nthreads) {
+    const int p0 = P.seq_pair[s], p1 = P.seq_pair[s + 1];
+    if (p1 > npairs) continue;
+    const int c = P.ctx[s];
+    int lq;
+    if (in.cu_seqlens_q) {
+      const int q0 = in.cu_seqlens_q[s];
+      lq = in.cu_seqlens_q[s + 1] - q0;
+      if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) lq = 0;
+    } else {
+      lq = c > 0 ? 1 : 0;
+    }
+    for (int p = p0; p < p1; ++p)
+      P.pair_off[p] = in.Hkv * pair_tiles(c, lq, p - p0, in.qtile, in.causal);
+  }
+  __syncthreads();
+  int total = block_exclusive_scan(P.pair_off, npairs, scratch);
+  if (tid == 0) P.pair_off[npairs] = total;
+  P.npairs = npairs;
+  P.total = total;
+  __syncthreads();
+}
+
+// q_len of sequence s as the plan sees it (0 for sequences it dropped).
+__device__ __forceinline__ int plan_qlen(const PlanSmem& P, const PlanInputs& in, int s) {
+  const int np = P.seq_pair[s + 1] - P.seq_pair[s];
+  if (np == 0) return 0;
+  return in.cu_seqlens_q ? (in.cu_seqlens_q[s + 1] - in.cu_seqlens_q[s]) : 1;
+}
+
+// Largest i in [lo, hi) with a[i] <= x (a non-decreasing, a[lo] <= x).
+__device__ __forceinline__ int upper_index(const int* a, int lo, int hi, int x) {
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (a[mid] <= x)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Position of one flat tile index.
+struct TilePos {
+  int s;    // sequence
+  int p;    // pair (sequence, query tile)
+  int qt;   // query tile within the sequence
+  int h;    // kv head
+  int b;    // key tile (block) within the segment
+  int nt;   // key tiles of the segment
+};
+
+__device__ __forceinline__ TilePos locate(const PlanSmem& P, int S, int Hkv, int idx) {
+  TilePos t;
+  t.p = upper_index(P.pair_off, 0, P.npairs, idx);
+  t.s = upper_index(P.seq_pair, 0, S, t.p);
+  t.qt = t.p - P.seq_pair[t.s];
+  t.nt = (P.pair_off[t.p + 1] - P.pair_off[t.p]) / Hkv;
+  const int local = idx - P.pair_off[t.p];
+  t.h = local / t.nt;
+  t.b = local - t.h * t.nt;
+  return t;
+}
+
+// Step a position to the next flat tile (only called while idx + 1 < total).
+__device__ __forceinline__ void advance(const PlanSmem& P, int S, int Hkv, TilePos& t) {
+  if (++t.b < t.nt) return;
+  t.b = 0;
+  if (++t.h < Hkv) return;
+  t.h = 0;
+  do {
+    ++t.p;
+  } while (P.pair_off[t.p + 1] == P.pair_off[t.p]);
+  while (P.seq_pair[t.s + 1] <= t.p) ++t.s;
+  t.qt = t.p - P.seq_pair[t.s];
+  t.nt = (P.pair_off[t.p + 1] - P.pair_off[t.p]) / Hkv;
+}
+
+}  // namespace pa

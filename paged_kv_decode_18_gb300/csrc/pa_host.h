@@ -1,0 +1,68 @@
+// pa_host.h -- host-side helpers shared by the translation units of
+// libpagedattn: status plumbing, shape checks, cached device properties.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int max_smem_optin = 0;  // bytes of dynamic shared memory a CTA may opt in to
+};
+
+// Properties of the current device (queried once per device, then cached).
+// Returns false if a CUDA call fails.
+inline bool current_device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev].device != dev) {
+    DeviceInfo d;
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return false;
+    cache[dev] = d;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Checks of the shape fields every call uses.
+inline int check_shape_common(const pa_shape* s) {
+  if (!s) return PA_ERR_ARG;
+  if (s->num_seqs < 0 || s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 ||
+      s->block_size <= 0 || s->max_blocks_per_seq < 0 || s->num_blocks < 0)
+    return PA_ERR_ARG;
+  if (s->num_q_heads % s->num_kv_heads != 0) return PA_ERR_ARG;
+  if (s->head_dim != 128 || s->block_size != 16) return PA_ERR_UNSUPPORTED;
+  // flat tile indices and slot numbers are kept in 32-bit ints
+  if (static_cast<int64_t>(s->max_blocks_per_seq) * s->block_size > (1 << 30)) return PA_ERR_ARG;
+  if (s->num_blocks * s->num_kv_heads * s->block_size >= (int64_t(1) << 40)) return PA_ERR_ARG;
+  return PA_OK;
+}
+
+// Each TU that owns kernels exposes the reader of its device error word.
+unsigned take_error_word_cache(cudaStream_t stream, int* rc);
+unsigned take_error_word_decode(cudaStream_t stream, int* rc);
+unsigned take_error_word_varlen(cudaStream_t stream, int* rc);
+
+}  // namespace pa

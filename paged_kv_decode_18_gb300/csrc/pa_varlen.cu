@@ -1,0 +1,609 @@
+// pa_varlen.cu -- paged attention for several query tokens per sequence:
+// speculative-decoding verify (1 + k draft tokens, causal inside the query
+// window) and chunked prefill (a chunk of queries at an offset whose earlier
+// tokens are already cached), over the same block pool as decode.
+//
+// Pages: "S20 - The Complete Engine", section "Core idea" (step 3 PROPOSE
+// attaches draft tokens, step 5 verifies them in the same forward); course
+// README "Build an LLM Inference Engine From Scratch", curriculum rows
+// "Batching & Scheduling" (chunked prefill, FlashAttention) and "Decoding
+// Acceleration" (speculative decoding), and its claim that online softmax is
+// exact and split-K variants agree.
+//
+// Query j of a sequence with q_len Lq and context c sits at position
+// c - Lq + j and (causal) sees keys 0 .. c - Lq + j.
+//
+// Design (GB300): q_len x group rows per KV head make QK^T and PV real
+// matrix products, so they run on the tensor cores (mma.sync m16n8k16, bf16
+// in, fp32 accumulate) in tiles of 16 rows = (16/G) query tokens x G query
+// heads of one KV head against 16-key blocks:
+//   * K/V tiles arrive by 2-D TMA (cp.async.bulk.tensor) with the 128-byte
+//     swizzle, so ldmatrix reads them without bank conflicts; the Q rows of a
+//     tile arrive by 1-D bulk copies when a new (sequence, query tile) starts;
+//   * one warp is one worker with a private ring of stages and a contiguous
+//     range of the batch's (sequence, query tile, KV head, block) tiles -- the
+//     same equal-range balancing as decode, so verify sequences, prefill
+//     chunks and ragged lengths spread evenly over the GPU;
+//   * online softmax on the accumulator fragments, P rounded to bf16 for the
+//     PV product (as FlashAttention does), running sums kept in fp32.
+#include <cudaTypedefs.h>
+
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+constexpr int kRows = 16;                      // rows of one query tile
+constexpr int kHalfBytes = kBlock * 128;       // 16 rows x 128 B (64 dims), swizzled
+constexpr int kQSlotBytes = kRows * kHeadDim * 2;  // 4 KB
+constexpr int kStageBytes = 4 * kHalfBytes + kQSlotBytes;  // K0 K1 V0 V1 Q = 12 KB
+constexpr int kDescInts = 8;
+
+struct VarlenArgs {
+  const uint16_t* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* cu_seqlens_q;
+  uint16_t* out;
+  float* lse;
+  float scale_log2;
+  int S, Hq, Hkv, G, QT, max_blocks;
+  int64_t num_blocks;
+  int64_t num_q_tokens;
+  int causal;
+  int npairs_cap;
+  int num_workers;
+  float* part_o;    // [NW*2][16][D]
+  float* part_lse;  // [NW*2][16]
+  int* desc;        // [NW][kDescInts]
+};
+
+// byte offset of (row, 16-byte chunk) inside a 16 x 128 B box written by TMA
+// with the 128-byte swizzle (chunk index XOR row mod 8)
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int NWARPS, int NSTAGE>
+__global__ void __launch_bounds__(NWARPS * 32)
+    paged_varlen_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const VarlenArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // stage buffers need 1024-byte alignment for the swizzle pattern
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* wbuf = smem + warp * (NSTAGE * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NWARPS * NSTAGE * kStageBytes) +
+                   warp * NSTAGE;
+  const int S = a.S, Hkv = a.Hkv, Hq = a.Hq, G = a.G, QT = a.QT;
+
+  int* pm = reinterpret_cast<int*>(smem + NWARPS * NSTAGE * kStageBytes + NWARPS * NSTAGE * 8);
+  PlanSmem P;
+  P.pair_off = pm;
+  P.seq_pair = P.pair_off + (a.npairs_cap + 1);
+  P.ctx = P.seq_pair + (S + 1);
+  P.qstart = P.ctx + S;
+  int* scratch = P.qstart + (S + 1);
+
+  if (lane == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    mbar_fence_init();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  PlanInputs in;
+  in.context_lens = a.context_lens;
+  in.cu_seqlens_q = a.cu_seqlens_q;
+  in.S = S;
+  in.Hkv = Hkv;
+  in.max_ctx = a.max_blocks * kBlock;
+  in.qtile = QT;
+  in.causal = a.causal;
+  in.npairs_cap = a.npairs_cap;
+  in.num_q_rows = a.num_q_tokens;
+  build_plan(in, P, scratch);
+
+  const int W = P.total;
+  const int w = blockIdx.x * NWARPS + warp;
+  const int nw = min(a.num_workers, W);
+  int R0 = 0, R1 = 0;
+  if (w < nw) {
+    R0 = (int)((int64_t)w * W / nw);
+    R1 = (int)((int64_t)(w + 1) * W / nw);
+  }
+  if (w < a.num_workers && lane == 0) {
+    int d[5] = {-1, 0, 0, 0, 0};
+    if (R0 < R1) {
+      const TilePos t = locate(P, S, Hkv, R0);
+      const int A = R0 - t.b;
+      const int R0prev = w > 0 ? (int)((int64_t)(w - 1) * W / nw) : 0;
+      if (t.b > 0 && A >= R0prev) {
+        d[0] = t.s;
+        d[1] = t.qt;
+        d[2] = t.h;
+        d[3] = (int)(((int64_t)(A + t.nt) * nw - 1) / W);
+        d[4] = (A == R0prev) ? 0 : 1;
+      }
+    }
+    int* dd = a.desc + (size_t)w * kDescInts;
+    for (int i = 0; i < 5; ++i) dd[i] = d[i];
+  }
+  if (R0 >= R1) return;
+
+  // ---- producer --------------------------------------------------------------
+  TilePos pp = locate(P, S, Hkv, R0);
+  int pidx = R0, wbase = R0;
+  auto load_phys = [&](int idx) -> int {
+    if (idx >= R1) return 0;
+    const TilePos t = locate(P, S, Hkv, idx);
+    return a.block_tables[(size_t)t.s * a.max_blocks + t.b];
+  };
+  int phys_cur = load_phys(wbase + lane);
+  int phys_next = load_phys(wbase + 32 + lane);
+
+  auto issue = [&](int stage) {
+    int phys = __shfl_sync(kFull, phys_cur, pidx - wbase);
+    const bool first = (pidx == R0) || (pp.b == 0);
+    if (lane == 0) {
+      if (phys < 0 || (int64_t)phys >= a.num_blocks) {
+        flag_error(PA_DEVERR_BLOCK_RANGE);
+        phys = 0;
+      }
+      unsigned char* st = wbuf + stage * kStageBytes;
+      const uint32_t bar = smem_addr(&bars[stage]);
+      int nq = 0;
+      if (first) {
+        const int lq = P.qstart[pp.s + 1] - P.qstart[pp.s];
+        nq = min(QT, lq - pp.qt * QT);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, 4 * kHalfBytes + nq * G * kHeadDim * 2);
+      const int y = (int)(((int64_t)phys * Hkv + pp.h) * kBlock);
+      tma_load_2d(smem_addr(st), &tmk, 0, y, bar);
+      tma_load_2d(smem_addr(st + kHalfBytes), &tmk, 64, y, bar);
+      tma_load_2d(smem_addr(st + 2 * kHalfBytes), &tmv, 0, y, bar);
+      tma_load_2d(smem_addr(st + 3 * kHalfBytes), &tmv, 64, y, bar);
+      const int64_t row0 = (int64_t)P.qstart[pp.s] + (int64_t)pp.qt * QT;
+      for (int j = 0; j < nq; ++j)
+        bulk_copy_g2s(smem_addr(st + 4 * kHalfBytes + j * G * kHeadDim * 2),
+                      a.q + ((row0 + j) * Hq + (int64_t)pp.h * G) * kHeadDim,
+                      G * kHeadDim * 2, bar);
+    }
+    ++pidx;
+    if (pidx < R1) advance(P, S, Hkv, pp);
+    if (pidx - wbase == 32) {
+      wbase += 32;
+      phys_cur = phys_next;
+      phys_next = load_phys(wbase + 32 + lane);
+    }
+  };
+
+  for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
+
+  // ---- consumer --------------------------------------------------------------
+  TilePos cp = locate(P, S, Hkv, R0);
+  const int r0 = lane >> 2, r1 = r0 + 8;  // the two accumulator rows of this lane
+  const int quad = lane & 3;
+  uint32_t qa[8][4];
+  float o[16][4];
+  float m_r[2], l_r[2];
+  int lim[2] = {0, 0}, lim_min = 0, lq = 0, ctx = 0;
+  int piece_b0 = 0;
+  bool piece_first = true;
+
+  int k = 0;
+  for (int idx = R0; idx < R1; ++idx, ++k) {
+    const int stage = k % NSTAGE;
+    const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
+    if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
+      for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
+        mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
+      return;
+    }
+    unsigned char* st = wbuf + stage * kStageBytes;
+    const uint32_t sK = smem_addr(st), sV = smem_addr(st + 2 * kHalfBytes);
+    const bool first = (idx == R0) || (cp.b == 0);
+    if (first) {
+      const uint32_t sQ = smem_addr(st + 4 * kHalfBytes);
+      const int mi = lane >> 3, rr = lane & 7;
+      const int qrow = (mi & 1) * 8 + rr;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        ldsm_x4(sQ + qrow * 256 + (2 * kk + (mi >> 1)) * 16, qa[kk][0], qa[kk][1], qa[kk][2],
+                qa[kk][3]);
+#pragma unroll
+      for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      m_r[0] = m_r[1] = neg_inf();
+      l_r[0] = l_r[1] = 0.f;
+      ctx = P.ctx[cp.s];
+      lq = P.qstart[cp.s + 1] - P.qstart[cp.s];
+      const int rows[2] = {r0, r1};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int tok = cp.qt * QT + rows[i] / G;
+        lim[i] = tok < lq ? (a.causal ? ctx - lq + tok + 1 : ctx) : 0;
+      }
+      int mn = min(lim[0], lim[1]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) mn = min(mn, __shfl_xor_sync(kFull, mn, off));
+      lim_min = mn;
+      piece_b0 = cp.b;
+      piece_first = (idx == R0);
+    }
+    const int key0 = cp.b * kBlock;
+    // keys past the context may hold anything: zero those V rows so that
+    // P = 0 never meets a NaN in the PV product
+    if (key0 + kBlock > ctx) {
+      const int zr = ctx - key0;  // first row to clear
+      for (int i = lane; i < (kBlock - zr) * 16; i += 32) {
+        const int row = zr + (i >> 4), c = i & 15;
+        *reinterpret_cast<uint4*>(st + 2 * kHalfBytes + (c >> 3) * kHalfBytes + row * 128 +
+                                  (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+
+    // ---- S = Q K^T (16 rows x 16 keys) -------------------------------------------
+    float s[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = (mi >> 1) * 8 + rr;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int c = 2 * kk + (mi & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sK + (c >> 3) * kHalfBytes + swz(key, c & 7), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qa[kk], b0, b1);
+        mma_bf16_16816(s[1], qa[kk], b2, b3);
+      }
+    }
+    // ---- mask, online softmax ----------------------------------------------------
+    const bool need_mask = key0 + kBlock > lim_min;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = s[n][e] * a.scale_log2;
+        if (need_mask) {
+          const int key = key0 + n * 8 + quad * 2 + (e & 1);
+          if (key >= lim[e >> 1]) v = neg_inf();
+        }
+        s[n][e] = v;
+      }
+    }
+    float alpha[2], mref[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float mx = fmaxf(fmaxf(s[0][2 * i], s[0][2 * i + 1]), fmaxf(s[1][2 * i], s[1][2 * i + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      const float mn = fmaxf(m_r[i], mx);
+      mref[i] = mn == neg_inf() ? 0.f : mn;
+      alpha[i] = ex2(m_r[i] - mref[i]);
+      m_r[i] = mn;
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = ex2(s[n][e] - mref[e >> 1]);
+        s[n][e] = p;
+        rs[e >> 1] += p;
+      }
+    }
+    l_r[0] = l_r[0] * alpha[0] + rs[0];
+    l_r[1] = l_r[1] * alpha[1] + rs[1];
+    if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= alpha[0];
+        o[n][1] *= alpha[0];
+        o[n][2] *= alpha[1];
+        o[n][3] *= alpha[1];
+      }
+    }
+    // ---- O += P V ----------------------------------------------------------------------
+    uint32_t pa4[4];
+    pa4[0] = cvt_bf16x2(s[0][0], s[0][1]);
+    pa4[1] = cvt_bf16x2(s[0][2], s[0][3]);
+    pa4[2] = cvt_bf16x2(s[1][0], s[1][1]);
+    pa4[3] = cvt_bf16x2(s[1][2], s[1][3]);
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = (mi & 1) * 8 + rr;
+#pragma unroll
+      for (int cpair = 0; cpair < 8; ++cpair) {
+        const int c = 2 * cpair + (mi >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(sV + (c >> 3) * kHalfBytes + swz(key, c & 7), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * cpair], pa4, b0, b1);
+        mma_bf16_16816(o[2 * cpair + 1], pa4, b2, b3);
+      }
+    }
+    __syncwarp();
+
+    if (pidx < R1) issue(stage);
+
+    const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
+    if (last) {
+      float lt[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float x = l_r[i];
+        x += __shfl_xor_sync(kFull, x, 1);
+        x += __shfl_xor_sync(kFull, x, 2);
+        lt[i] = x;
+      }
+      const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
+      const int rows[2] = {r0, r1};
+      if (complete) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int tok = cp.qt * QT + rows[i] / G;
+          if (tok >= lq) continue;
+          const int g = rows[i] % G;
+          const int64_t orow = ((int64_t)P.qstart[cp.s] + tok) * Hq + (int64_t)cp.h * G + g;
+          const float inv = lt[i] > 0.f ? 1.f / lt[i] : 0.f;
+          uint16_t* dst = a.out + orow * kHeadDim + quad * 2;
+#pragma unroll
+          for (int n = 0; n < 16; ++n)
+            *reinterpret_cast<uint32_t*>(dst + n * 8) =
+                cvt_bf16x2(o[n][2 * i] * inv, o[n][2 * i + 1] * inv);
+          if (a.lse && quad == 0)
+            a.lse[orow] = lt[i] > 0.f ? (m_r[i] + lg2(lt[i])) * kLn2 : neg_inf();
+        }
+      } else {
+        const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float inv = lt[i] > 0.f ? 1.f / lt[i] : 0.f;
+          float* dst = a.part_o + (slot * kRows + rows[i]) * kHeadDim + quad * 2;
+#pragma unroll
+          for (int n = 0; n < 16; ++n)
+            *reinterpret_cast<float2*>(dst + n * 8) =
+                make_float2(o[n][2 * i] * inv, o[n][2 * i + 1] * inv);
+          if (quad == 0)
+            a.part_lse[slot * kRows + rows[i]] =
+                lt[i] > 0.f ? (m_r[i] + lg2(lt[i])) * kLn2 : neg_inf();
+        }
+      }
+    }
+    if (idx + 1 < R1) advance(P, S, Hkv, cp);
+  }
+}
+
+// Merge the pieces of (sequence, query tile, KV head) segments cut by the
+// balanced ranges; one warp per worker boundary, rows looped.
+__global__ void varlen_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
+                                    const float* __restrict__ part_lse,
+                                    const int32_t* __restrict__ cu_seqlens_q, int num_workers,
+                                    int Hq, int G, int QT, uint16_t* __restrict__ out,
+                                    float* __restrict__ lse) {
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= num_workers) return;
+  const int* d = desc + (size_t)w * kDescInts;
+  const int s = d[0];
+  if (s < 0) return;
+  const int qt = d[1], h = d[2], last = d[3], slot_prev = d[4];
+  const int q0 = cu_seqlens_q[s], lq = cu_seqlens_q[s + 1] - q0;
+  for (int r = 0; r < kRows; ++r) {
+    const int tok = qt * QT + r / G;
+    if (tok >= lq) continue;
+    float mx = neg_inf();
+    for (int x = w - 1; x <= last; ++x) {
+      const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+      mx = fmaxf(mx, part_lse[slot * kRows + r]);
+    }
+    float sum = 0.f;
+    for (int x = w - 1; x <= last; ++x) {
+      const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+      sum += ex2((part_lse[slot * kRows + r] - mx) * kLog2e);
+    }
+    const float LSE = mx + lg2(sum) * kLn2;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int x = w - 1; x <= last; ++x) {
+      const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+      const float wt = ex2((part_lse[slot * kRows + r] - LSE) * kLog2e);
+      const float4 v =
+          *reinterpret_cast<const float4*>(part_o + (slot * kRows + r) * kHeadDim + lane * 4);
+      acc.x = fmaf(wt, v.x, acc.x);
+      acc.y = fmaf(wt, v.y, acc.y);
+      acc.z = fmaf(wt, v.z, acc.z);
+      acc.w = fmaf(wt, v.w, acc.w);
+    }
+    const int64_t orow = ((int64_t)q0 + tok) * Hq + (int64_t)h * G + r % G;
+    uint2 ov;
+    ov.x = cvt_bf16x2(acc.x, acc.y);
+    ov.y = cvt_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(out + orow * kHeadDim + lane * 4) = ov;
+    if (lse && lane == 0) lse[orow] = LSE;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+constexpr int kWarps = 4;
+constexpr int kStages = 2;
+
+struct VarlenGeometry {
+  int grid = 0, workers = 0, npairs_cap = 0;
+  size_t smem = 0, ws_desc = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
+};
+
+int varlen_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
+                    VarlenGeometry* g) {
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return PA_ERR_CUDA;
+  const int S = sh->num_seqs;
+  const int G = sh->num_q_heads / sh->num_kv_heads, QT = kRows / G;
+  const int64_t cap1 = (int64_t)S * ((max_q_len + QT - 1) / QT);
+  const int64_t cap2 = (num_q_tokens + QT - 1) / QT + S;
+  const int64_t cap = cap1 < cap2 ? cap1 : cap2;
+  if (cap > (1 << 22)) return PA_ERR_UNSUPPORTED;
+  g->npairs_cap = (int)(cap < 1 ? 1 : cap);
+  const size_t plan = sizeof(int) * ((size_t)g->npairs_cap + 1 + 3 * (size_t)S + 2 + 40);
+  g->smem = 1024 + (size_t)kWarps * kStages * kStageBytes + (size_t)kWarps * kStages * 8 + plan;
+  if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
+  auto kern = paged_varlen_kernel<kWarps, kStages>;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g->smem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, g->smem) !=
+          cudaSuccess ||
+      per_sm <= 0)
+    return PA_ERR_CUDA;
+  g->grid = dev.num_sms * per_sm;
+  g->workers = g->grid * kWarps;
+  g->ws_desc = round_up(sizeof(int) * kDescInts * (size_t)g->workers, 256);
+  g->ws_lse = round_up(sizeof(float) * 2 * kRows * (size_t)g->workers, 256);
+  g->ws_o = round_up(sizeof(float) * 2 * kRows * kHeadDim * (size_t)g->workers, 256);
+  g->ws_bytes = g->ws_desc + g->ws_lse + g->ws_o;
+  return PA_OK;
+}
+
+int check_varlen_args(const pa_shape* shape, int64_t num_q_tokens, int max_q_len) {
+  int rc = check_shape_common(shape);
+  if (rc != PA_OK) return rc;
+  const int G = shape->num_q_heads / shape->num_kv_heads;
+  if (G > kRows || kRows % G != 0) return PA_ERR_UNSUPPORTED;
+  if (num_q_tokens < 0 || max_q_len < 0) return PA_ERR_ARG;
+  if (num_q_tokens > 0x3fffffff) return PA_ERR_ARG;
+  if (shape->num_blocks * shape->num_kv_heads * kBlock > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// 2-D view of one pool array: [num_blocks * Hkv * 16 rows][128] bf16, boxes of
+// 16 rows x 64 dims, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+unsigned take_error_word_varlen(cudaStream_t stream, int* rc) {
+  unsigned v = 0, zero = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&v, g_pa_error_word, sizeof v) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_pa_error_word, &zero, sizeof zero) != cudaSuccess) {
+    *rc = PA_ERR_CUDA;
+    return 0;
+  }
+  return v;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_varlen_workspace_size(const pa_shape* shape, int64_t num_q_tokens,
+                                                  int max_q_len) {
+  if (check_varlen_args(shape, num_q_tokens, max_q_len) != PA_OK) return 0;
+  if (shape->num_seqs == 0 || num_q_tokens == 0) return 0;
+  VarlenGeometry g;
+  if (varlen_geometry(shape, num_q_tokens, max_q_len, &g) != PA_OK) return 0;
+  return g.ws_bytes;
+}
+
+extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* cu_seqlens_q, int64_t num_q_tokens,
+                                int max_q_len, int causal, float scale, pa_bf16* out, float* lse,
+                                const pa_shape* shape, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  int rc = check_varlen_args(shape, num_q_tokens, max_q_len);
+  if (rc != PA_OK) return rc;
+  if (shape->num_seqs == 0 || num_q_tokens == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !cu_seqlens_q || !out)
+    return PA_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(cu_seqlens_q, 4) ||
+      (lse && !aligned(lse, 4)))
+    return PA_ERR_ARG;
+  if (!(scale == scale)) return PA_ERR_ARG;
+  VarlenGeometry g;
+  rc = varlen_geometry(shape, num_q_tokens, max_q_len, &g);
+  if (rc != PA_OK) return rc;
+  if (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256))
+    return PA_ERR_WORKSPACE;
+  const int64_t rows = shape->num_blocks * shape->num_kv_heads * kBlock;
+  CUtensorMap tmk, tmv;
+  if (!make_pool_map(&tmk, k_cache, rows) || !make_pool_map(&tmv, v_cache, rows))
+    return PA_ERR_CUDA;
+
+  VarlenArgs a;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.out = out;
+  a.lse = lse;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.S = shape->num_seqs;
+  a.Hq = shape->num_q_heads;
+  a.Hkv = shape->num_kv_heads;
+  a.G = a.Hq / a.Hkv;
+  a.QT = kRows / a.G;
+  a.max_blocks = shape->max_blocks_per_seq;
+  a.num_blocks = shape->num_blocks;
+  a.num_q_tokens = num_q_tokens;
+  a.causal = causal ? 1 : 0;
+  a.npairs_cap = g.npairs_cap;
+  a.num_workers = g.workers;
+  char* ws = static_cast<char*>(workspace);
+  a.desc = reinterpret_cast<int*>(ws);
+  a.part_lse = reinterpret_cast<float*>(ws + g.ws_desc);
+  a.part_o = reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  paged_varlen_kernel<kWarps, kStages><<<g.grid, kWarps * 32, g.smem, st>>>(tmk, tmv, a);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  const int wpb = 8;
+  varlen_fixup_kernel<<<(g.workers + wpb - 1) / wpb, wpb * 32, 0, st>>>(
+      a.desc, a.part_o, a.part_lse, cu_seqlens_q, g.workers, a.Hq, a.G, a.QT, out, lse);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}

@@ -1,0 +1,92 @@
+"""Helpers for the GPU parity tests: the device side of a workload goes
+through the CUDA library only (the pool is written by the CUDA cache-write
+kernel); the reference side through the oracle only."""
+import numpy as np
+import torch
+
+from paged_kv_decode_18_gb300 import binding as B
+
+OUT_ATOL = 1e-2
+OUT_RTOL = 1e-2
+LSE_ATOL = 1e-3
+
+
+def device():
+    if not torch.cuda.is_available():
+        raise RuntimeError("GPU test needs CUDA")
+    return torch.device("cuda:0")
+
+
+class DeviceBatch:
+    """A workload's tensors on the GPU, with its pool filled by the CUDA cache
+    write (history first, then the step's new tokens)."""
+
+    def __init__(self, w, dev=None, write_new=True):
+        dev = dev or device()
+        self.w = w
+        self.dev = dev
+        self.kc, self.vc = w.empty_pool(dev)
+        self.q = w.q.to(dev)
+        self.k_new = w.k_new.to(dev)
+        self.v_new = w.v_new.to(dev)
+        self.slot_new = w.slot_new.to(dev)
+        self.block_tables = w.block_tables.to(dev)
+        self.context_lens = w.context_lens.to(dev)
+        self.cu_seqlens_q = w.cu_seqlens_q.to(dev)
+        if w.k_hist.shape[0]:
+            B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
+                                   self.kc, self.vc)
+        if write_new:
+            self.write_new()
+
+    def write_new(self):
+        B.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_new, self.kc, self.vc)
+
+    def pools_u16(self):
+        return (self.kc.cpu().view(torch.int16).numpy().view(np.uint16),
+                self.vc.cpu().view(torch.int16).numpy().view(np.uint16))
+
+    def decode(self, num_splits=0, with_lse=True):
+        out = torch.empty_like(self.q)
+        lse = (torch.empty(self.q.shape[:2], dtype=torch.float32, device=self.dev)
+               if with_lse else None)
+        sh = B.shape_of(self.q, self.kc, self.block_tables)
+        ws = B.workspace(B.pa_decode_workspace_size(sh, num_splits), self.dev)
+        B.pa_decode(self.q, self.kc, self.vc, self.block_tables, self.context_lens,
+                    self.w.scale, out, lse, num_splits=num_splits, workspace=ws)
+        return out, lse
+
+    def varlen(self, causal=True, with_lse=True):
+        out = torch.empty_like(self.q)
+        lse = (torch.empty(self.q.shape[:2], dtype=torch.float32, device=self.dev)
+               if with_lse else None)
+        sh = B.shape_of(self.q, self.kc, self.block_tables)
+        mq = self.w.max_q_len
+        ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, self.q.shape[0], mq), self.dev)
+        B.pa_decode_varlen(self.q, self.kc, self.vc, self.block_tables, self.context_lens,
+                           self.cu_seqlens_q, mq, self.w.scale, out, lse, causal=causal,
+                           workspace=ws)
+        return out, lse
+
+
+def assert_attention_close(out, lse, ref_out, ref_lse, rows=None, what=""):
+    """|gpu - ref| <= 1e-2 + 1e-2 |ref| for out (bf16 vs fp64), |dlse| <= 1e-3."""
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref_o = ref_out
+    if rows is not None:
+        got, ref_o = got[rows], ref_o[rows]
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref_o)
+    tol = OUT_ATOL + OUT_RTOL * np.abs(ref_o)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} out elements beyond tolerance, "
+                           f"worst {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")
+    if lse is not None:
+        gl = lse.cpu().numpy().astype(np.float64)
+        rl = ref_lse
+        if rows is not None:
+            gl, rl = gl[rows], rl[rows]
+        inf = np.isinf(rl)
+        assert np.array_equal(np.isinf(gl), inf), f"{what}: -inf rows differ"
+        lerr = np.abs(gl[~inf] - rl[~inf])
+        assert lerr.size == 0 or lerr.max() <= LSE_ATOL, f"{what}: lse err {lerr.max():.3e}"

@@ -1,0 +1,131 @@
+"""CUDA paged decode (q_len 1) vs the fp64 oracle on the same seeded inputs:
+|out - ref| <= 1e-2 + 1e-2 |ref| and |lse - ref| <= 1e-3, over every split
+mode, at reduced sizes that span several tiles with ragged tails and at the
+full sizes of the workloads (the benchmark's launch configuration is
+num_splits = 0)."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_decode_18_gb300 import binding as B
+from paged_kv_decode_18_gb300 import build as libbuild
+from paged_kv_decode_18_gb300 import workloads as W
+from tests.gpu_util import DeviceBatch, assert_attention_close
+from tests.pools import oracle_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    libbuild.build()
+    B.load()
+
+
+CASES = {
+    "tiny": ("tiny", {}),
+    "engine": ("engine", {}),
+    "ragged_small": ("ragged", dict(num_seqs=40, max_context=700)),
+    "ragged_full": ("ragged", {}),
+    "long_small": ("long", dict(num_seqs=2, context=3000)),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_decode_matches_oracle(case, num_splits):
+    name, sizes = CASES[case]
+    w = W.make(name, seed=11, **sizes)
+    db = DeviceBatch(w)
+    out, lse = db.decode(num_splits)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what=f"{case}/splits={num_splits}")
+
+
+@pytest.mark.parametrize("num_splits", [0, 16, 32, 64])
+def test_long_context_full_size(num_splits):
+    # batch 8 x 32768 tokens, 1% outlier keys x8, split-K 16..64 or balanced
+    w = W.long(seed=12)
+    db = DeviceBatch(w)
+    out, lse = db.decode(num_splits)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what=f"long/splits={num_splits}")
+
+
+def test_split_modes_agree():
+    w = W.ragged(seed=13, num_seqs=64, max_context=2000)
+    db = DeviceBatch(w)
+    outs = [db.decode(p) for p in (0, 1, 2, 7)]
+    base = outs[1][0].float()
+    for o, l in outs:
+        assert (o.float() - base).abs().max().item() <= 2e-2
+        assert (l - outs[1][1]).abs().max().item() <= 1e-4
+
+
+def test_deterministic_and_workspace_reuse():
+    w = W.engine(seed=14)
+    db = DeviceBatch(w)
+    o1, l1 = db.decode(0)
+    o2, l2 = db.decode(0)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def test_lse_optional():
+    w = W.tiny(seed=15)
+    db = DeviceBatch(w)
+    o1, _ = db.decode(0, with_lse=False)
+    o2, _ = db.decode(0, with_lse=True)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 4])
+def test_empty_context_rows(num_splits):
+    w = W.tiny(seed=16)
+    db = DeviceBatch(w)
+    db.context_lens[1] = 0
+    out, lse = db.decode(num_splits)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    ref, ref_lse = oracle_attention(w)
+    rows = [0, 2, 3]
+    assert_attention_close(out, lse, ref, ref_lse, rows=rows, what="non-empty rows")
+
+
+def test_bad_block_id_is_flagged_not_read():
+    w = W.tiny(seed=17)
+    db = DeviceBatch(w)
+    B.pa_debug_read_error()
+    db.block_tables[0, 0] = w.num_blocks + 5
+    db.block_tables[2, 3] = -7
+    out, lse = db.decode(0)
+    err = B.pa_debug_read_error()
+    assert err & B.PA_DEVERR_BLOCK_RANGE
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, rows=[1, 3], what="untouched rows")
+
+
+def test_context_past_table_is_flagged():
+    w = W.tiny(seed=18)
+    db = DeviceBatch(w)
+    B.pa_debug_read_error()
+    db.context_lens[0] = w.max_blocks_per_seq * w.block_size + 1
+    db.decode(0)
+    assert B.pa_debug_read_error() & B.PA_DEVERR_CONTEXT_RANGE
+
+
+def test_workspace_too_small_is_rejected():
+    w = W.tiny(seed=19)
+    db = DeviceBatch(w)
+    sh = B.shape_of(db.q, db.kc, db.block_tables)
+    need = B.pa_decode_workspace_size(sh, 0)
+    small = torch.empty(need // 2, dtype=torch.uint8, device=db.dev)
+    out = torch.empty_like(db.q)
+    with pytest.raises(B.PAError) as e:
+        B.pa_decode(db.q, db.kc, db.vc, db.block_tables, db.context_lens, w.scale, out,
+                    num_splits=0, workspace=small)
+    assert e.value.status == B.PA_ERR_WORKSPACE
