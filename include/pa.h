@@ -146,6 +146,32 @@ int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
 size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits);
 
 /*
+ * pa_decode_static_scratch -- pa_decode with num_splits == 0 (balanced split)
+ * that allocates nothing and takes no workspace. The source pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory themselves -- a plugin inside another runtime that owns every device
+ * allocation, or a serving loop whose memory is planned once up front (where a
+ * cudaMalloc would also synchronise the device).
+ *
+ * Arguments, layouts and results are those of pa_decode. The split scratch is
+ * a fixed 4 MiB array inside the library (static device memory that every GPU
+ * loading the library holds until the process exits). A shape whose balanced
+ * split needs more than 4 MiB on the current device returns PA_ERR_WORKSPACE
+ * (use pa_decode with a workspace instead); on a 152-SM GB300 the need is
+ * about 2.5 MiB for any batch. The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls share the one
+ * array and its contents carry over between calls (nothing in it needs to
+ * start at zero): calls that may overlap on the GPU -- on different streams,
+ * or from different host threads -- race on it and must be serialised by the
+ * caller.
+ */
+int pa_decode_static_scratch(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                             void* stream);
+
+/*
  * pa_decode_varlen -- several query tokens per sequence over the same paged
  * pool: speculative-decoding verify (1 + k draft tokens, causal within the
  * query window; "S20 - The Complete Engine", step 3 PROPOSE and step 5

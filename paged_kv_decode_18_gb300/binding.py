@@ -37,6 +37,7 @@ EXPORTED = (
     "pa_reshape_and_cache",
     "pa_decode",
     "pa_decode_workspace_size",
+    "pa_decode_static_scratch",
     "pa_decode_varlen",
     "pa_decode_varlen_workspace_size",
     "pa_splitk_reduce",
@@ -88,6 +89,8 @@ def load(path: str | None = None):
         lib.pa_decode.argtypes = [V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
         lib.pa_decode_workspace_size.restype = sz
         lib.pa_decode_workspace_size.argtypes = [S, i32]
+        lib.pa_decode_static_scratch.restype = i32
+        lib.pa_decode_static_scratch.argtypes = [V, V, V, V, V, f32, V, V, S, V]
         lib.pa_decode_varlen.restype = i32
         lib.pa_decode_varlen.argtypes = [V, V, V, V, V, V, i64, i32, i32, f32, V, V, S, V, sz, V]
         lib.pa_decode_varlen_workspace_size.restype = sz
@@ -213,6 +216,30 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=N
                             _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
                             ctypes.byref(sh), int(num_splits), _ptr(workspace), ws_bytes,
                             _stream(stream)), "pa_decode")
+
+
+def pa_decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                             lse=None, stream=None) -> None:
+    """pa_decode (balanced split) without a workspace, for callers that cannot
+    allocate device memory: the split scratch is a fixed 4 MiB array inside the
+    library. Calls that may overlap on the GPU share that array and race."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    sh = shape_of(q, k_cache, block_tables)
+    if q.shape[0] != sh.num_seqs or context_lens.shape[0] != sh.num_seqs:
+        raise ValueError("q / context_lens rows != number of sequences")
+    if out.shape != q.shape:
+        raise ValueError("out shape != q shape")
+    _check(load().pa_decode_static_scratch(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(block_tables), _ptr(context_lens), float(scale),
+                                           _ptr(out), _ptr(lse), ctypes.byref(sh),
+                                           _stream(stream)), "pa_decode_static_scratch")
 
 
 def pa_decode_varlen_workspace_size(shape: pa_shape, num_q_tokens: int, max_q_len: int) -> int:

@@ -692,3 +692,62 @@ extern "C" int pa_splitk_reduce(const float* part_out, const float* part_lse, in
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// pa_decode_static_scratch: pa_decode (balanced split) for callers that are
+// not allowed to allocate device memory themselves -- for example a plugin
+// running inside another runtime that owns every device allocation, or a
+// serving loop whose memory is planned once up front, where a cudaMalloc would
+// also synchronise the device. Its split scratch is this file-scope array
+// instead of a caller workspace. The array is part of the library image: every
+// GPU that loads the library holds these bytes until the process exits.
+// ---------------------------------------------------------------------------
+namespace pa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_pa_static_scratch[kStaticScratchBytes];
+
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a host-side stand-in, so the real address is looked up
+// once per device (with that device current) and cached.
+void* static_scratch_address(int* rc) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *rc = PA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || p == nullptr) {
+      *rc = PA_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_static_scratch(const pa_bf16* q, const pa_bf16* k_cache,
+                                        const pa_bf16* v_cache, const int32_t* block_tables,
+                                        const int32_t* context_lens, float scale, pa_bf16* out,
+                                        float* lse, const pa_shape* shape, void* stream) {
+  int rc = check_decode_args(shape, 0);
+  if (rc != PA_OK) return rc;
+  if (shape->num_seqs == 0) return PA_OK;
+  DecodeGeometry g;
+  rc = decode_geometry(shape, 0, &g);
+  if (rc != PA_OK) return rc;
+  if (g.ws_bytes > kStaticScratchBytes) return PA_ERR_WORKSPACE;  // beyond the fixed array
+  rc = PA_OK;
+  void* scratch = static_scratch_address(&rc);
+  if (scratch == nullptr) return rc;
+  return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape, 0,
+                   scratch, kStaticScratchBytes, stream);
+}
