@@ -4,7 +4,7 @@ One step = one attention layer's decode step of the engine-shaped batch
 (64 sequences, context 384, q_len 1, 16 query / 8 KV heads, head_dim 128,
 block 16, bf16): the slot-mapped write of the 64 new tokens' K/V into the
 block pool, then paged decode attention over the pool (balanced split with
-its merge). Inputs are device resident when the timed region starts; the
+its merge) -- one ``pa_append_decode`` call (three kernels). Inputs are device resident when the timed region starts; the
 e2e figure instead moves each step's inputs from pinned host memory and
 reads the result back, through the library's public calls.
 
@@ -211,8 +211,11 @@ def run_ours(args, rank, world, dev):
     if B.pa_debug_read_error() != 0:
         raise RuntimeError("device error while filling the pools")
 
-    def write(l):
-        B.pa_reshape_and_cache(bufs["k_new"], bufs["v_new"], bufs["slot_new"], l.kc, l.vc)
+    def step(l):
+        # the whole step in one call: cache write of the new tokens, then decode
+        B.pa_append_decode(bufs["k_new"], bufs["v_new"], bufs["slot_new"], bufs["q"], l.kc, l.vc,
+                           bufs["block_tables"], bufs["context_lens"], w.scale, out, lse,
+                           workspace=ws)
 
     def decode(l):
         B.pa_decode(bufs["q"], l.kc, l.vc, bufs["block_tables"], bufs["context_lens"],
@@ -223,50 +226,53 @@ def run_ours(args, rank, world, dev):
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for l in layers:
-            write(l)
+            step(l)
             decode(l)
     stream.wait_stream(side)
     graphs = []
     for l in layers:
-        gw, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gw):
-            write(l)
+        gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs):
+            step(l)
         with torch.cuda.graph(gd):
             decode(l)
-        graphs.append((gw, gd))
+        graphs.append((gs, gd))
     torch.cuda.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device() if dev.index is None else dev.index)
     clocks.start()
     for i in range(args.warmup):
-        gw, gd = graphs[i % LAYERS]
-        gw.replay()
+        gs, gd = graphs[i % LAYERS]
+        gs.replay()
         gd.replay()
     torch.cuda.synchronize()
 
+    def timed(K, which):
+        """Per-replay CUDA-event times (ms) of K replays of graph `which`."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        chunk = 256
+        for c0 in range(0, K, chunk):
+            # park the stream briefly so the host can queue a chunk of steps ahead
+            torch.cuda._sleep(2_000_000)
+            for i in range(c0, min(K, c0 + chunk)):
+                ev[i][0].record(stream)
+                graphs[i % LAYERS][which].replay()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.mark()
-    chunk = 256
-    for c0 in range(0, K, chunk):
-        # park the stream briefly so the host can queue a chunk of steps ahead
-        torch.cuda._sleep(2_000_000)
-        for i in range(c0, min(K, c0 + chunk)):
-            gw, gd = graphs[i % LAYERS]
-            ev[i][0].record(stream)
-            gw.replay()
-            ev[i][1].record(stream)
-            gd.replay()
-            ev[i][2].record(stream)
-    torch.cuda.synchronize()
+    step_ms = timed(K, 0)
     clocks.mark()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    # the dominant call on its own, for the roofline
+    dec_ms = timed(min(K, 2000), 1)
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     clk = clocks.stop()
     err = B.pa_debug_read_error()
@@ -314,9 +320,9 @@ def run_e2e(args, w, dev, B, layers, ws):
     def step(l):
         for k in names:
             devb[k].copy_(host[k], non_blocking=True)
-        B.pa_reshape_and_cache(devb["k_new"], devb["v_new"], devb["slot_new"], l.kc, l.vc)
-        B.pa_decode(devb["q"], l.kc, l.vc, devb["block_tables"], devb["context_lens"], w.scale,
-                    out, lse, num_splits=0, workspace=ws)
+        B.pa_append_decode(devb["k_new"], devb["v_new"], devb["slot_new"], devb["q"], l.kc, l.vc,
+                           devb["block_tables"], devb["context_lens"], w.scale, out, lse,
+                           workspace=ws)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
         torch.cuda.current_stream().synchronize()  # the result is read on the host

@@ -146,6 +146,24 @@ int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
 size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits);
 
 /*
+ * pa_append_decode -- one decode step of one attention layer in one call:
+ * pa_reshape_and_cache(k_new, v_new, slot_mapping, num_new_tokens, ...)
+ * followed by pa_decode(..., num_splits = 0, ...) ("KV Cache > The Idea":
+ * append the new K/V, then attend over the whole history). Same arguments,
+ * layouts, results and workspace (pa_decode_workspace_size(shape, 0)) as the
+ * two calls. The decode grid is queued as a programmatic dependent of the
+ * cache-write grid and prepares its work (reading context_lens and
+ * block_tables) while the write runs; it reads the pool only after the write
+ * has finished. So context_lens and block_tables must not alias k_new, v_new,
+ * slot_mapping or the pool.
+ */
+int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new, const int64_t* slot_mapping,
+                     int64_t num_new_tokens, const pa_bf16* q, pa_bf16* k_cache,
+                     pa_bf16* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                     float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_decode_static_scratch -- pa_decode with num_splits == 0 (balanced split)
  * that allocates nothing and takes no workspace. The source pages have no
  * counterpart: this entry point exists for callers that cannot allocate device

@@ -38,6 +38,7 @@ EXPORTED = (
     "pa_decode",
     "pa_decode_workspace_size",
     "pa_decode_static_scratch",
+    "pa_append_decode",
     "pa_decode_varlen",
     "pa_decode_varlen_workspace_size",
     "pa_splitk_reduce",
@@ -89,6 +90,8 @@ def load(path: str | None = None):
         lib.pa_decode.argtypes = [V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
         lib.pa_decode_workspace_size.restype = sz
         lib.pa_decode_workspace_size.argtypes = [S, i32]
+        lib.pa_append_decode.restype = i32
+        lib.pa_append_decode.argtypes = [V, V, V, i64, V, V, V, V, V, f32, V, V, S, V, sz, V]
         lib.pa_decode_static_scratch.restype = i32
         lib.pa_decode_static_scratch.argtypes = [V, V, V, V, V, f32, V, V, S, V]
         lib.pa_decode_varlen.restype = i32
@@ -216,6 +219,36 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=N
                             _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
                             ctypes.byref(sh), int(num_splits), _ptr(workspace), ws_bytes,
                             _stream(stream)), "pa_decode")
+
+
+def pa_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                     context_lens, scale, out, lse=None, workspace=None, stream=None) -> None:
+    """Cache write of the step's new K/V rows, then decode (balanced split), as
+    one call whose decode preparation overlaps the write."""
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    if k_new.shape != v_new.shape or slot_mapping.shape[0] != k_new.shape[0]:
+        raise ValueError("k_new / v_new / slot_mapping disagree")
+    sh = shape_of(q, k_cache, block_tables)
+    if q.shape[0] != sh.num_seqs or context_lens.shape[0] != sh.num_seqs:
+        raise ValueError("q / context_lens rows != number of sequences")
+    if out.shape != q.shape:
+        raise ValueError("out shape != q shape")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_append_decode(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0],
+                                   _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                   _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
+                                   ctypes.byref(sh), _ptr(workspace), ws_bytes,
+                                   _stream(stream)), "pa_append_decode")
 
 
 def pa_decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale, out,

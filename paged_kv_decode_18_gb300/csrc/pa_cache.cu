@@ -19,6 +19,9 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
                                          const int64_t* __restrict__ slots, int64_t total_chunks,
                                          int Hkv, int64_t num_slots, uint4* __restrict__ k_cache,
                                          uint4* __restrict__ v_cache) {
+  // a dependent grid queued behind this one (decode in pa_append_decode) may
+  // start its own preparation now; it waits for this grid before reading the pool
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= total_chunks) return;
   const int per_token = Hkv * kChunksPerRow;

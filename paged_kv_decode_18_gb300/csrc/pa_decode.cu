@@ -18,11 +18,13 @@
 //     with a 1-D bulk async copy (TMA engine) onto the stage's mbarrier, plus
 //     the 512 B of the two query heads when a new sequence starts;
 //   * both query heads of the KV head share every tile read from shared memory;
-//   * QK^T: lane (c, half) holds dims 8c..8c+7 for 8 tokens and both heads;
-//     the 16 partial dots are reduce-scattered over 16 lanes (15 shuffles)
-//     so each lane ends with one (token, head) score;
+//   * QK^T: lane (g, c) holds dims 16c..16c+15 of 4 tokens for both heads;
+//     the 8 partial dots are reduce-scattered over 8 lanes (7 shuffles) so
+//     each lane ends with one (token, head) score; fp32 pairs run through the
+//     packed f32x2 FMA pipe of sm_100+;
 //   * online softmax in the log2 domain (scale * log2 e folded into q);
-//   * PV: the same lane layout accumulates 2 heads x 8 dims in fp32.
+//   * PV: the same lane layout accumulates 2 heads x 16 dims in fp32 pairs;
+//     the 4 token groups are combined through shared memory once per piece.
 // A batch is cut into equal tile ranges over all resident warps (num_splits
 // 0), so ragged batches and long contexts balance; a (sequence, KV head) cut
 // by a range boundary leaves partials that a small merge kernel combines.
@@ -63,12 +65,8 @@ struct DecodeArgs {
   float* part_o;    // kBalanced: [NW*2][G][D]; kFixed: [S][Hq][P][D]
   float* part_lse;  // kBalanced: [NW*2][G];    kFixed: [S][Hq][P]
   int* desc;        // kBalanced: [NW][kDescInts]
+  int early;        // 1: plan and table reads may run before the previous grid ends
 };
-
-__device__ __forceinline__ void unpack8(const uint4 w, float (&f)[8]) {
-  f[0] = bf_lo(w.x); f[1] = bf_hi(w.x); f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
-  f[4] = bf_lo(w.z); f[5] = bf_hi(w.z); f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
-}
 
 // Write 8 dims (one lane's chunk) of one output row as bf16.
 __device__ __forceinline__ void store_out8(uint16_t* dst, const float (&v)[8], float inv) {
@@ -92,7 +90,6 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* wbuf = smem + warp * L::kBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + L::kBarOff);
-  float* pbuf = reinterpret_cast<float*>(wbuf + L::kPOff);
   const int S = a.S, Hkv = a.Hkv, Hq = a.Hq;
 
   int* pm = reinterpret_cast<int*>(smem + NWARPS * L::kBytes);
@@ -107,6 +104,13 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_addr(&bars[i]), 1);
     mbar_fence_init();
   }
+  // This grid is launched as a programmatic dependent of the previous one on
+  // the stream. By default it waits for that grid right here, before reading
+  // anything. With `early` (used only behind this library's own cache-write
+  // kernel, which writes nothing but the pool) the plan, the block-table
+  // window and the merge descriptors are prepared first and the wait sits
+  // just before the first copy out of the pool.
+  if (!a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   PlanInputs in;
   in.context_lens = a.context_lens;
   in.cu_seqlens_q = nullptr;
@@ -118,6 +122,9 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   in.npairs_cap = S;
   in.num_q_rows = S;
   build_plan(in, P, scratch);  // ends with __syncthreads: barrier inits visible too
+  // the merge grid that follows may be scheduled from now on (it waits for
+  // this grid to finish before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int W = P.total;
   const int w = blockIdx.x * NWARPS + warp;
@@ -136,29 +143,11 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   }
 
   int R0 = 0, R1 = 0, fixed_p = 0;
+  const int nw = min(a.num_workers, W);
   if (a.mode == kBalanced) {
-    const int nw = min(a.num_workers, W);
     if (w < nw) {
       R0 = (int)((int64_t)w * W / nw);
       R1 = (int)((int64_t)(w + 1) * W / nw);
-    }
-    if (w < a.num_workers && lane == 0) {
-      // Does this worker own the merge of the segment its range starts in?
-      int d[5] = {-1, 0, 0, 0, 0};
-      if (R0 < R1) {
-        const TilePos t = locate(P, S, Hkv, R0);
-        const int A = R0 - t.b;  // flat start of the segment
-        const int R0prev = w > 0 ? (int)((int64_t)(w - 1) * W / nw) : 0;
-        if (t.b > 0 && A >= R0prev) {
-          const int B = A + t.nt;
-          d[0] = t.s;
-          d[1] = t.h;
-          d[2] = (int)(((int64_t)B * nw - 1) / W);  // worker holding the last tile
-          d[3] = (A == R0prev) ? 0 : 1;              // slot of worker w-1's piece
-        }
-      }
-      int* dd = a.desc + (size_t)w * kDescInts;
-      for (int i = 0; i < 5; ++i) dd[i] = d[i];
     }
   } else {
     const int PS = a.num_splits;
@@ -187,11 +176,14 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     R0 = P.pair_off[pr] + h * nt + b0;
     R1 = R0 + (b1 - b0);
   }
-  if (R0 >= R1) return;
+  if (R0 >= R1) {
+    if (a.mode == kBalanced && w < a.num_workers && lane == 0) a.desc[(size_t)w * kDescInts] = -1;
+    return;
+  }
 
-  const int c16 = lane & 15;  // dims 8*c16 .. 8*c16+7
-  const int th = lane >> 4;   // tokens 8*th .. 8*th+7 of a tile
-  const int hsel = lane & 1;  // head of the score this lane ends up holding
+  const int grp = lane >> 3;   // tokens 4*grp .. 4*grp+3 of a tile
+  const int c8 = lane & 7;     // dims 16*c8 .. 16*c8+15
+  const int hsel = lane & 1;   // head of the score this lane ends up holding
 
   // ---- producer state -----------------------------------------------------
   TilePos pp = locate(P, S, Hkv, R0);
@@ -233,12 +225,32 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     }
   };
 
+  if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
 
+  if (a.mode == kBalanced && lane == 0) {
+    // Does this worker own the merge of the segment its range starts in?
+    int d[5] = {-1, 0, 0, 0, 0};
+    const TilePos t = locate(P, S, Hkv, R0);
+    const int A = R0 - t.b;  // flat start of the segment
+    const int R0prev = w > 0 ? (int)((int64_t)(w - 1) * W / nw) : 0;
+    if (t.b > 0 && A >= R0prev) {
+      const int B = A + t.nt;
+      d[0] = t.s;
+      d[1] = t.h;
+      d[2] = (int)(((int64_t)B * nw - 1) / W);  // worker holding the last tile
+      d[3] = (A == R0prev) ? 0 : 1;              // slot of worker w-1's piece
+    }
+    int* dd = a.desc + (size_t)w * kDescInts;
+    for (int i = 0; i < 5; ++i) dd[i] = d[i];
+  }
+
   // ---- consumer -------------------------------------------------------------
+  // Lane (grp, c8) holds dims 16*c8..16*c8+15 of tokens 4*grp..4*grp+3 for
+  // both query heads; fp32 pairs go through the packed (f32x2) FMA pipe.
   TilePos cp = locate(P, S, Hkv, R0);
-  float qf[kG][8];
-  float acc[kG][8];
+  float2 q2[kG][8];    // scaled q, dims (16*c8 + 2j, +1)
+  float2 acc[kG][8];   // output accumulator, same dims
   float m0 = neg_inf(), m1 = neg_inf(), l_lane = 0.f;
   int piece_b0 = 0;
   bool piece_first = true;
@@ -253,19 +265,19 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
         mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
       return;
     }
-    const unsigned char* st = wbuf + stage * kStageBytes;
+    unsigned char* st = wbuf + stage * kStageBytes;
     const bool first = (idx == R0) || (cp.b == 0);
     if (first) {
-      const uint4 q0 = *reinterpret_cast<const uint4*>(st + 2 * kTileBytes + c16 * 16);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(st + 2 * kTileBytes + 256 + c16 * 16);
-      unpack8(q0, qf[0]);
-      unpack8(q1, qf[1]);
 #pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        qf[0][d] *= a.scale_log2;
-        qf[1][d] *= a.scale_log2;
-        acc[0][d] = 0.f;
-        acc[1][d] = 0.f;
+      for (int g = 0; g < kG; ++g) {
+        const uint4* qs = reinterpret_cast<const uint4*>(st + 2 * kTileBytes + g * 256 + c8 * 32);
+        const uint4 qa = qs[0], qb = qs[1];
+        const uint32_t wq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          q2[g][j] = make_float2(bf_lo(wq[j]) * a.scale_log2, bf_hi(wq[j]) * a.scale_log2);
+          acc[g][j] = make_float2(0.f, 0.f);
+        }
       }
       m0 = neg_inf();
       m1 = neg_inf();
@@ -275,28 +287,29 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     }
     const int nvalid = min(kBlock, P.ctx[cp.s] - cp.b * kBlock);
 
-    // ---- scores: 8 tokens x 2 heads of partial dots per lane ---------------
-    float sc[16];
-    const unsigned char* Ks = st + th * 8 * 256 + c16 * 16;
+    // ---- scores: 4 tokens x 2 heads of partial dots per lane ----------------
+    float sc[8];
+    const unsigned char* Ks = st + grp * 4 * 256 + c8 * 32;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint4 kw = *reinterpret_cast<const uint4*>(Ks + i * 256);
-      float kf[8];
-      unpack8(kw, kf);
-      float d0 = 0.f, d1 = 0.f;
+    for (int i = 0; i < 4; ++i) {
+      const uint4 ka = *reinterpret_cast<const uint4*>(Ks + i * 256);
+      const uint4 kb = *reinterpret_cast<const uint4*>(Ks + i * 256 + 16);
+      const uint32_t wk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+      float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        d0 = fmaf(qf[0][d], kf[d], d0);
-        d1 = fmaf(qf[1][d], kf[d], d1);
+      for (int j = 0; j < 8; ++j) {
+        const float2 kf = make_float2(bf_lo(wk[j]), bf_hi(wk[j]));
+        d0 = __ffma2_rn(q2[0][j], kf, d0);
+        d1 = __ffma2_rn(q2[1][j], kf, d1);
       }
-      sc[2 * i] = d0;
-      sc[2 * i + 1] = d1;
+      sc[2 * i] = d0.x + d0.y;
+      sc[2 * i + 1] = d1.x + d1.y;
     }
-    // reduce-scatter over the 16 lanes of this half-warp: value v = 2*i + g
-    // ends in the lane with (lane & 15) == v
+    // reduce-scatter over the 8 lanes of this group: value v = 2*i + g ends in
+    // the lane with (lane & 7) == v
 #pragma unroll
-    for (int step = 0; step < 4; ++step) {
-      const int half = 8 >> step;
+    for (int step = 0; step < 3; ++step) {
+      const int half = 4 >> step;
       const bool upper = (lane & half) != 0;
 #pragma unroll
       for (int j = 0; j < half; ++j) {
@@ -305,8 +318,8 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
         sc[j] = keep + __shfl_xor_sync(kFull, send, half);
       }
     }
-    const int tok = th * 8 + ((lane & 15) >> 1);
-    float s_val = tok < nvalid ? sc[0] : neg_inf();
+    const int tok = grp * 4 + ((lane & 7) >> 1);
+    const float s_val = tok < nvalid ? sc[0] : neg_inf();
 
     // ---- online softmax (log2 domain) ------------------------------------------
     float mx = s_val;
@@ -320,115 +333,116 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     m1 = mn1;
     const float p = ex2(s_val - (hsel ? mn1 : mn0));
     l_lane = l_lane * (hsel ? al1 : al0) + p;
-    pbuf[lane] = p;  // index 2*token_in_half + head, halves at 0 and 16
+    float* pbuf = reinterpret_cast<float*>(wbuf + L::kPOff);
+    pbuf[lane] = p;  // index 2*token + head
     __syncwarp();
-    float pv[16];
+    float pv[8];
     {
-      const float4* pb = reinterpret_cast<const float4*>(pbuf + th * 16);
-      const float4 p0 = pb[0], p1 = pb[1], p2 = pb[2], p3 = pb[3];
+      const float4* pb = reinterpret_cast<const float4*>(pbuf + grp * 8);
+      const float4 p0 = pb[0], p1 = pb[1];
       pv[0] = p0.x; pv[1] = p0.y; pv[2] = p0.z; pv[3] = p0.w;
       pv[4] = p1.x; pv[5] = p1.y; pv[6] = p1.z; pv[7] = p1.w;
-      pv[8] = p2.x; pv[9] = p2.y; pv[10] = p2.z; pv[11] = p2.w;
-      pv[12] = p3.x; pv[13] = p3.y; pv[14] = p3.z; pv[15] = p3.w;
     }
     if (al0 != 1.f || al1 != 1.f) {
+      const float2 a0 = make_float2(al0, al0), a1 = make_float2(al1, al1);
 #pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        acc[0][d] *= al0;
-        acc[1][d] *= al1;
+      for (int j = 0; j < 8; ++j) {
+        acc[0][j] = __fmul2_rn(acc[0][j], a0);
+        acc[1][j] = __fmul2_rn(acc[1][j], a1);
       }
     }
     // ---- PV ----------------------------------------------------------------------
-    const unsigned char* Vs = st + kTileBytes + th * 8 * 256 + c16 * 16;
-    if (nvalid == kBlock) {
+    const unsigned char* Vs = st + kTileBytes + grp * 4 * 256 + c8 * 32;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 vw = *reinterpret_cast<const uint4*>(Vs + i * 256);
-        float vf[8];
-        unpack8(vw, vf);
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-          acc[0][d] = fmaf(pv[2 * i], vf[d], acc[0][d]);
-          acc[1][d] = fmaf(pv[2 * i + 1], vf[d], acc[1][d]);
-        }
-      }
-    } else {
+    for (int i = 0; i < 4; ++i) {
       // tokens past the context may hold anything (even NaN): skip, never 0*x
+      if (nvalid == kBlock || grp * 4 + i < nvalid) {
+        const uint4 va = *reinterpret_cast<const uint4*>(Vs + i * 256);
+        const uint4 vb = *reinterpret_cast<const uint4*>(Vs + i * 256 + 16);
+        const uint32_t wv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        const float2 p0 = make_float2(pv[2 * i], pv[2 * i]);
+        const float2 p1 = make_float2(pv[2 * i + 1], pv[2 * i + 1]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (th * 8 + i < nvalid) {
-          const uint4 vw = *reinterpret_cast<const uint4*>(Vs + i * 256);
-          float vf[8];
-          unpack8(vw, vf);
-#pragma unroll
-          for (int d = 0; d < 8; ++d) {
-            acc[0][d] = fmaf(pv[2 * i], vf[d], acc[0][d]);
-            acc[1][d] = fmaf(pv[2 * i + 1], vf[d], acc[1][d]);
-          }
+        for (int j = 0; j < 8; ++j) {
+          const float2 vf = make_float2(bf_lo(wv[j]), bf_hi(wv[j]));
+          acc[0][j] = __ffma2_rn(p0, vf, acc[0][j]);
+          acc[1][j] = __ffma2_rn(p1, vf, acc[1][j]);
         }
       }
     }
-    __syncwarp();  // all lanes are done with this stage and with pbuf
-
-    if (pidx < R1) issue(stage);
+    __syncwarp();  // all lanes are done with this stage's K/V and with pbuf
 
     const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
     if (last) {
-      // ---- finish the piece -------------------------------------------------------
+      // ---- finish the piece: combine the 4 token groups through this stage's
+      // (already consumed) K buffer, then each lane owns 8 outputs ------------
+      float* red = reinterpret_cast<float*>(st);  // [grp][g][128] fp32 = 4 KB
 #pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        acc[0][d] += __shfl_xor_sync(kFull, acc[0][d], 16);
-        acc[1][d] += __shfl_xor_sync(kFull, acc[1][d], 16);
+      for (int g = 0; g < kG; ++g) {
+        float4* dst = reinterpret_cast<float4*>(red + (grp * kG + g) * kHeadDim + c8 * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(acc[g][2 * j].x, acc[g][2 * j].y, acc[g][2 * j + 1].x,
+                               acc[g][2 * j + 1].y);
       }
       float ls = l_lane;
 #pragma unroll
       for (int o = 2; o < 32; o <<= 1) ls += __shfl_xor_sync(kFull, ls, o);
       const float lo = __shfl_xor_sync(kFull, ls, 1);
       const float l0 = hsel ? lo : ls, l1 = hsel ? ls : lo;
+      __syncwarp();
+      const int og = lane >> 4;          // output head of this lane
+      const int od = (lane & 15) * 8;    // output dims od .. od+7
+      float o8[8];
+      {
+        const float4* r0 = reinterpret_cast<const float4*>(red + og * kHeadDim + od);
+        float4 x = r0[0], y = r0[1];
+#pragma unroll
+        for (int gg = 1; gg < 4; ++gg) {
+          const float4* r = reinterpret_cast<const float4*>(red + (gg * kG + og) * kHeadDim + od);
+          const float4 u = r[0], v = r[1];
+          x.x += u.x; x.y += u.y; x.z += u.z; x.w += u.w;
+          y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+        }
+        o8[0] = x.x; o8[1] = x.y; o8[2] = x.z; o8[3] = x.w;
+        o8[4] = y.x; o8[5] = y.y; o8[6] = y.z; o8[7] = y.w;
+      }
+      const float lsum = og ? l1 : l0;
+      const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
+      const float inv = 1.f / lsum;
       const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
-      const float lse0 = (m0 + lg2(l0)) * kLn2, lse1 = (m1 + lg2(l1)) * kLn2;
-      const size_t row0 = (size_t)cp.s * Hq + (size_t)cp.h * kG;
+      const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
       if (a.mode == kFixed && a.num_splits > 1) {
         const int PS = a.num_splits;
-        if (th == 0) {
-          store_f8(a.part_o + ((row0 + 0) * PS + fixed_p) * kHeadDim + c16 * 8, acc[0], 1.f / l0);
-          store_f8(a.part_o + ((row0 + 1) * PS + fixed_p) * kHeadDim + c16 * 8, acc[1], 1.f / l1);
-        }
-        if (lane == 0) {
-          a.part_lse[(row0 + 0) * PS + fixed_p] = lse0;
-          a.part_lse[(row0 + 1) * PS + fixed_p] = lse1;
-        }
+        store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
+        if ((lane & 15) == 0) a.part_lse[row * PS + fixed_p] = lse_own;
       } else if (complete) {
-        if (th == 0) {
-          store_out8(a.out + (row0 + 0) * kHeadDim + c16 * 8, acc[0], 1.f / l0);
-          store_out8(a.out + (row0 + 1) * kHeadDim + c16 * 8, acc[1], 1.f / l1);
-        }
-        if (a.lse && lane == 0) {
-          a.lse[row0 + 0] = lse0;
-          a.lse[row0 + 1] = lse1;
-        }
+        store_out8(a.out + row * kHeadDim + od, o8, inv);
+        if (a.lse && (lane & 15) == 0) a.lse[row] = lse_own;
       } else {
         const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
-        if (th == 0) {
-          store_f8(a.part_o + (slot * kG + 0) * kHeadDim + c16 * 8, acc[0], 1.f / l0);
-          store_f8(a.part_o + (slot * kG + 1) * kHeadDim + c16 * 8, acc[1], 1.f / l1);
-        }
-        if (lane == 0) {
-          a.part_lse[slot * kG + 0] = lse0;
-          a.part_lse[slot * kG + 1] = lse1;
-        }
+        store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
+        if ((lane & 15) == 0) a.part_lse[slot * kG + og] = lse_own;
       }
+      __syncwarp();  // the reduction buffer is read before the refill lands
     }
+
+    if (pidx < R1) issue(stage);
     if (idx + 1 < R1) advance(P, S, Hkv, cp);
   }
 }
 
 // Merge the pieces of every (sequence, KV head) that the balanced ranges cut.
 // One warp per worker boundary; the owner recorded in desc[w] merges the
-// pieces held by workers w-1 .. last.
-__global__ void decode_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
-                                    const float* __restrict__ part_lse, int num_workers, int Hq,
-                                    uint16_t* __restrict__ out, float* __restrict__ lse) {
+// pieces held by workers w-1 .. last. Lane i reads piece i's lse values, so
+// the maxima and sums take one round of loads and a few shuffles; the partial
+// vectors are then loaded several pieces at a time. Launched as a dependent
+// grid: it may start while the decode kernel drains and waits for it here.
+__global__ void __launch_bounds__(256)
+    decode_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
+                        const float* __restrict__ part_lse, int num_workers, int Hq,
+                        uint16_t* __restrict__ out, float* __restrict__ lse) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= num_workers) return;
@@ -436,32 +450,64 @@ __global__ void decode_fixup_kernel(const int* __restrict__ desc, const float* _
   const int s = d[0];
   if (s < 0) return;
   const int h = d[1], last = d[2], slot_prev = d[3];
-  float mx[kG], sum[kG], LSE[kG];
-  for (int g = 0; g < kG; ++g) mx[g] = neg_inf();
-  for (int x = w - 1; x <= last; ++x) {
-    const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
-    for (int g = 0; g < kG; ++g) mx[g] = fmaxf(mx[g], part_lse[slot * kG + g]);
-  }
-  for (int g = 0; g < kG; ++g) sum[g] = 0.f;
-  for (int x = w - 1; x <= last; ++x) {
-    const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
-    for (int g = 0; g < kG; ++g) sum[g] += ex2((part_lse[slot * kG + g] - mx[g]) * kLog2e);
-  }
-  for (int g = 0; g < kG; ++g) LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
+  const int npieces = last - w + 2;  // workers w-1 .. last
   float4 acc[kG];
   for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int x = w - 1; x <= last; ++x) {
-    const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
+  float LSE[kG];
+  // pass 1: log-sum-exp over all pieces (32 pieces per round)
+  float mx[kG] = {neg_inf(), neg_inf()}, sum[kG] = {0.f, 0.f};
+  for (int i0 = 0; i0 < npieces; i0 += 32) {
+    const int i = i0 + lane;
+    float li[kG] = {neg_inf(), neg_inf()};
+    if (i < npieces) {
+      const size_t slot = (size_t)(w - 1 + i) * 2 + (i == 0 ? slot_prev : 0);
+      const float2 v = *reinterpret_cast<const float2*>(part_lse + slot * kG);
+      li[0] = v.x;
+      li[1] = v.y;
+    }
+#pragma unroll
     for (int g = 0; g < kG; ++g) {
-      const float wt = ex2((part_lse[slot * kG + g] - LSE[g]) * kLog2e);
-      const float4 o =
-          *reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4);
-      acc[g].x = fmaf(wt, o.x, acc[g].x);
-      acc[g].y = fmaf(wt, o.y, acc[g].y);
-      acc[g].z = fmaf(wt, o.z, acc[g].z);
-      acc[g].w = fmaf(wt, o.w, acc[g].w);
+      float m = li[g];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      const float mnew = fmaxf(mx[g], m);
+      float e = ex2((li[g] - mnew) * kLog2e);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(kFull, e, o);
+      sum[g] = sum[g] * ex2((mx[g] - mnew) * kLog2e) + e;
+      mx[g] = mnew;
     }
   }
+#pragma unroll
+  for (int g = 0; g < kG; ++g) LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
+  // pass 2: weighted sum of the partial outputs
+  for (int i0 = 0; i0 < npieces; i0 += 32) {
+    const int i = i0 + lane;
+    float wl[kG] = {0.f, 0.f};
+    if (i < npieces) {
+      const size_t slot = (size_t)(w - 1 + i) * 2 + (i == 0 ? slot_prev : 0);
+      const float2 v = *reinterpret_cast<const float2*>(part_lse + slot * kG);
+      wl[0] = ex2((v.x - LSE[0]) * kLog2e);
+      wl[1] = ex2((v.y - LSE[1]) * kLog2e);
+    }
+    const int n = min(32, npieces - i0);
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const int ii = i0 + j;
+      const size_t slot = (size_t)(w - 1 + ii) * 2 + (ii == 0 ? slot_prev : 0);
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        const float wt = __shfl_sync(kFull, wl[g], j);
+        const float4 o =
+            *reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4);
+        acc[g].x = fmaf(wt, o.x, acc[g].x);
+        acc[g].y = fmaf(wt, o.y, acc[g].y);
+        acc[g].z = fmaf(wt, o.z, acc[g].z);
+        acc[g].w = fmaf(wt, o.w, acc[g].w);
+      }
+    }
+  }
+#pragma unroll
   for (int g = 0; g < kG; ++g) {
     const size_t row = (size_t)s * Hq + (size_t)h * kG + g;
     uint2 o;
@@ -615,10 +661,15 @@ extern "C" size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits
   return g.ws_bytes;
 }
 
-extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
-                         const int32_t* block_tables, const int32_t* context_lens, float scale,
-                         pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+namespace pa {
+namespace {
+
+// Validate, size and launch the decode grid and its merge. `early`: see the
+// kernel (only pa_append_decode sets it).
+int decode_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, float scale,
+                pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+                void* workspace, size_t workspace_bytes, cudaStream_t st, int early) {
   int rc = check_decode_args(shape, num_splits);
   if (rc != PA_OK) return rc;
   if (shape->num_seqs == 0) return PA_OK;
@@ -651,26 +702,75 @@ extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
   a.mode = g.mode;
   a.num_splits = g.P;
   a.num_workers = g.workers;
+  a.early = early;
   char* ws = static_cast<char*>(workspace);
   a.desc = g.ws_desc ? reinterpret_cast<int*>(ws) : nullptr;
   a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
   a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  paged_decode_kernel<kWarps, kStages><<<g.grid, kWarps * 32, g.smem, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_dependent(paged_decode_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
+                       g.smem, st, a) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int wpb = 8;
   if (g.mode == kBalanced) {
-    const int wpb = 8;
-    decode_fixup_kernel<<<(g.workers + wpb - 1) / wpb, wpb * 32, 0, st>>>(
-        a.desc, a.part_o, a.part_lse, g.workers, a.Hq, out, lse);
+    // the merge grid may be scheduled while the decode grid drains; it waits
+    // for the decode grid's completion before reading
+    if (launch_dependent(decode_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32), 0,
+                         st, (const int*)a.desc, (const float*)a.part_o,
+                         (const float*)a.part_lse, g.workers, a.Hq, (uint16_t*)out,
+                         lse) != cudaSuccess)
+      return PA_ERR_CUDA;
   } else if (g.P > 1) {
     const int64_t nrh = (int64_t)a.S * a.Hq;
-    const int wpb = 8;
     splitk_reduce_kernel<<<(unsigned)((nrh + wpb - 1) / wpb), wpb * 32, 0, st>>>(
         a.part_o, a.part_lse, nrh, g.P, kHeadDim, out, lse);
   }
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                         pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape,
+                     num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                     0);
+}
+
+extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
+                                const int64_t* slot_mapping, int64_t num_new_tokens,
+                                const pa_bf16* q, pa_bf16* k_cache, pa_bf16* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  // check everything first so that a failing call enqueues nothing
+  int rc = check_decode_args(shape, 0);
+  if (rc != PA_OK) return rc;
+  if (num_new_tokens < 0) return PA_ERR_ARG;
+  if (num_new_tokens > 0 &&
+      (!k_new || !v_new || !slot_mapping || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+       !aligned(slot_mapping, 8)))
+    return PA_ERR_ARG;
+  if (shape->num_seqs > 0) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
+    DecodeGeometry g;
+    rc = decode_geometry(shape, 0, &g);
+    if (rc != PA_OK) return rc;
+    if (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256))
+      return PA_ERR_WORKSPACE;
+  }
+  rc = pa_reshape_and_cache(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, shape,
+                            stream);
+  if (rc != PA_OK) return rc;
+  // with new tokens, the cache write ran just before: the decode prologue
+  // (which reads only context_lens and block_tables) may overlap it
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape, 0,
+                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                     num_new_tokens > 0 ? 1 : 0);
 }
 
 extern "C" int pa_splitk_reduce(const float* part_out, const float* part_lse, int64_t num_rows,

@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pa.h"
+#include "pa.h"
 
 namespace pa {
 
@@ -210,42 +210,29 @@ struct PlanInputs {
   int64_t num_q_rows;  // rows of q / out; every sequence's rows must lie inside
 };
 
-// Exclusive scan of n ints in shared memory, in place, by the whole CTA.
-// Returns the total. Uses `scratch` (>= 33 ints) for the warp partials.
-__device__ inline int block_exclusive_scan(int* data, int n, int* scratch) {
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int chunk = (n + nthreads - 1) / nthreads;
-  const int b = min(n, tid * chunk), e = min(n, b + chunk);
+// Exclusive scan of n ints in shared memory, in place, by warp 0 of the CTA
+// (each lane scans a contiguous chunk, then the lanes' totals are scanned by
+// shuffles). The caller synchronises the CTA before and after. Returns the
+// total in warp 0's lanes.
+__device__ inline int warp0_exclusive_scan(int* data, int n) {
+  const int lane = threadIdx.x & 31;
+  const int chunk = (n + 31) / 32;
+  const int b = min(n, lane * chunk), e = min(n, b + chunk);
   int local = 0;
   for (int i = b; i < e; ++i) local += data[i];
-  // inclusive scan of `local` across the CTA
-  const int lane = tid & 31, warp = tid >> 5, nwarps = (nthreads + 31) >> 5;
   int x = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(kFull, x, o);
+    const int y = __shfl_up_sync(kFull, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int wv = lane < nwarps ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(kFull, wv, o);
-      if (lane >= o) wv += y;
-    }
-    if (lane < nwarps) scratch[lane] = wv;  // inclusive warp totals
-  }
-  __syncthreads();
-  int run = x - local + (warp > 0 ? scratch[warp - 1] : 0);  // exclusive start
+  const int total = __shfl_sync(kFull, x, 31);
+  int run = x - local;
   for (int i = b; i < e; ++i) {
-    int v = data[i];
+    const int v = data[i];
     data[i] = run;
     run += v;
   }
-  const int total = scratch[nwarps - 1];
-  __syncthreads();
   return total;
 }
 
@@ -255,71 +242,75 @@ __device__ __forceinline__ int pair_tiles(int c, int lq, int qt, int qtile, int 
   return (kv_end + kBlock - 1) / kBlock;
 }
 
-// Build the plan in shared memory. All threads of the CTA must call it.
-// Invalid lengths are clamped (and flagged) so that every later access stays
-// inside the caller's buffers.
-__device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* scratch) {
+// Build the plan in shared memory. All threads of the CTA must call it; it
+// ends with a CTA barrier. Invalid lengths are clamped (and flagged) so that
+// every later access stays inside the caller's buffers.
+//
+// Decode (no cu_seqlens_q): pair p is sequence p (a sequence with an empty
+// context is a pair with no tiles), so one scan suffices.
+__device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scratch*/) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int S = in.S;
+  const bool varlen = in.cu_seqlens_q != nullptr;
   for (int s = tid; s < S; s += nthreads) {
     int c = in.context_lens[s];
     if (c < 0 || c > in.max_ctx) {
       flag_error(PA_DEVERR_CONTEXT_RANGE);
       c = c < 0 ? 0 : in.max_ctx;
     }
-    int lq = 1, q0 = s;
-    if (in.cu_seqlens_q) {
-      q0 = in.cu_seqlens_q[s];
-      lq = in.cu_seqlens_q[s + 1] - q0;
+    P.ctx[s] = c;
+    if (varlen) {
+      const int q0 = in.cu_seqlens_q[s];
+      int lq = in.cu_seqlens_q[s + 1] - q0;
       if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) {
         flag_error(PA_DEVERR_QLEN_RANGE);
         lq = 0;  // the sequence produces no rows
       }
-    } else if (c == 0) {
-      lq = 0;  // decode with an empty context: written separately as 0 / -inf
-    }
-    P.ctx[s] = c;
-    P.qstart[s] = q0;
-    P.seq_pair[s] = (lq + in.qtile - 1) / in.qtile;  // query tiles of s
-    if (s == S - 1) P.qstart[S] = in.cu_seqlens_q ? in.cu_seqlens_q[S] : S;
-  }
-  __syncthreads();
-  int npairs = block_exclusive_scan(P.seq_pair, S, scratch);
-  if (tid == 0) P.seq_pair[S] = npairs;
-  if (npairs > in.npairs_cap) {
-    if (tid == 0) flag_error(PA_DEVERR_PLAN_OVERFLOW);
-    npairs = 0;  // do nothing rather than overflow the shared arrays
-  }
-  __syncthreads();
-  // tiles per pair (times Hkv)
-  for (int s = tid; s < S; s += nthreads) {
-    const int p0 = P.seq_pair[s], p1 = P.seq_pair[s + 1];
-    if (p1 > npairs) continue;
-    const int c = P.ctx[s];
-    int lq;
-    if (in.cu_seqlens_q) {
-      const int q0 = in.cu_seqlens_q[s];
-      lq = in.cu_seqlens_q[s + 1] - q0;
-      if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) lq = 0;
+      P.qstart[s] = q0;
+      P.seq_pair[s] = (lq + in.qtile - 1) / in.qtile;  // query tiles of s
+      if (s == S - 1) P.qstart[S] = in.cu_seqlens_q[S];
     } else {
-      lq = c > 0 ? 1 : 0;
+      P.qstart[s] = s;
+      P.seq_pair[s] = s;
+      P.pair_off[s] = in.Hkv * ((c + kBlock - 1) / kBlock);
+      if (s == S - 1) {
+        P.qstart[S] = S;
+        P.seq_pair[S] = S;
+      }
     }
-    for (int p = p0; p < p1; ++p)
-      P.pair_off[p] = in.Hkv * pair_tiles(c, lq, p - p0, in.qtile, in.causal);
   }
   __syncthreads();
-  int total = block_exclusive_scan(P.pair_off, npairs, scratch);
-  if (tid == 0) P.pair_off[npairs] = total;
-  P.npairs = npairs;
-  P.total = total;
+  int npairs = S;
+  if (varlen) {
+    if (tid < 32) {
+      const int n = warp0_exclusive_scan(P.seq_pair, S);
+      if (tid == 0) P.seq_pair[S] = n;
+    }
+    __syncthreads();
+    npairs = P.seq_pair[S];
+    if (npairs > in.npairs_cap) {
+      if (tid == 0) flag_error(PA_DEVERR_PLAN_OVERFLOW);
+      npairs = 0;  // do nothing rather than overflow the shared arrays
+    }
+    for (int s = tid; s < S; s += nthreads) {
+      const int p0 = P.seq_pair[s], p1 = P.seq_pair[s + 1];
+      if (p1 > npairs) continue;
+      const int c = P.ctx[s];
+      const int q0 = in.cu_seqlens_q[s];
+      int lq = in.cu_seqlens_q[s + 1] - q0;
+      if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) lq = 0;
+      for (int p = p0; p < p1; ++p)
+        P.pair_off[p] = in.Hkv * pair_tiles(c, lq, p - p0, in.qtile, in.causal);
+    }
+    __syncthreads();
+  }
+  if (tid < 32) {
+    const int total = warp0_exclusive_scan(P.pair_off, npairs);
+    if (tid == 0) P.pair_off[npairs] = total;
+  }
   __syncthreads();
-}
-
-// q_len of sequence s as the plan sees it (0 for sequences it dropped).
-__device__ __forceinline__ int plan_qlen(const PlanSmem& P, const PlanInputs& in, int s) {
-  const int np = P.seq_pair[s + 1] - P.seq_pair[s];
-  if (np == 0) return 0;
-  return in.cu_seqlens_q ? (in.cu_seqlens_q[s + 1] - in.cu_seqlens_q[s]) : 1;
+  P.npairs = npairs;
+  P.total = P.pair_off[npairs];
 }
 
 // Largest i in [lo, hi) with a[i] <= x (a non-decreasing, a[lo] <= x).

@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/pa.h"
+#include "pa.h"
 
 namespace pa {
 
@@ -58,6 +58,24 @@ inline int check_shape_common(const pa_shape* s) {
   if (static_cast<int64_t>(s->max_blocks_per_seq) * s->block_size > (1 << 30)) return PA_ERR_ARG;
   if (s->num_blocks * s->num_kv_heads * s->block_size >= (int64_t(1) << 40)) return PA_ERR_ARG;
   return PA_OK;
+}
+
+// Launch a kernel as a programmatic dependent of the previous grid on the
+// stream (it may start before that grid ends and waits inside).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // Each TU that owns kernels exposes the reader of its device error word.

@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(NWARPS * 32)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
+  // launched as a programmatic dependent of the previous grid: wait for it
+  // before reading anything it may have written
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   PlanInputs in;
   in.context_lens = a.context_lens;
   in.cu_seqlens_q = a.cu_seqlens_q;
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(NWARPS * 32)
   in.npairs_cap = a.npairs_cap;
   in.num_q_rows = a.num_q_tokens;
   build_plan(in, P, scratch);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int W = P.total;
   const int w = blockIdx.x * NWARPS + warp;
@@ -215,6 +219,18 @@ __global__ void __launch_bounds__(NWARPS * 32)
     const bool first = (idx == R0) || (cp.b == 0);
     if (first) {
       const uint32_t sQ = smem_addr(st + 4 * kHalfBytes);
+      ctx = P.ctx[cp.s];
+      lq = P.qstart[cp.s + 1] - P.qstart[cp.s];
+      // rows of query tokens past the sequence's last one are padding: zero
+      // them so they stay finite (they are never written out)
+      const int nq = min(QT, lq - cp.qt * QT);
+      if (nq < QT) {
+        unsigned char* qpad = st + 4 * kHalfBytes + nq * G * kHeadDim * 2;
+        const int chunks = (QT - nq) * G * kHeadDim * 2 / 16;
+        for (int i = lane; i < chunks; i += 32)
+          reinterpret_cast<uint4*>(qpad)[i] = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+      }
       const int mi = lane >> 3, rr = lane & 7;
       const int qrow = (mi & 1) * 8 + rr;
 #pragma unroll
@@ -225,15 +241,17 @@ __global__ void __launch_bounds__(NWARPS * 32)
       for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
       m_r[0] = m_r[1] = neg_inf();
       l_r[0] = l_r[1] = 0.f;
-      ctx = P.ctx[cp.s];
-      lq = P.qstart[cp.s + 1] - P.qstart[cp.s];
       const int rows[2] = {r0, r1};
+      // key limit of each row; padding rows (zero Q) need none
+      int lv[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int tok = cp.qt * QT + rows[i] / G;
-        lim[i] = tok < lq ? (a.causal ? ctx - lq + tok + 1 : ctx) : 0;
+        const bool valid = tok < lq;
+        lim[i] = valid ? (a.causal ? ctx - lq + tok + 1 : ctx) : 0x7fffffff;
+        lv[i] = valid ? lim[i] : 0x7fffffff;
       }
-      int mn = min(lim[0], lim[1]);
+      int mn = min(lv[0], lv[1]);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) mn = min(mn, __shfl_xor_sync(kFull, mn, off));
       lim_min = mn;
@@ -255,9 +273,13 @@ __global__ void __launch_bounds__(NWARPS * 32)
 
     // ---- S = Q K^T (16 rows x 16 keys) -------------------------------------------
     float s[2][4];
-#pragma unroll
-    for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
     {
+      // two independent accumulation chains per key group (even / odd k-steps)
+      float sx[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[n][e] = sx[n][e] = 0.f;
       const int mi = lane >> 3, rr = lane & 7;
       const int key = (mi >> 1) * 8 + rr;
 #pragma unroll
@@ -265,9 +287,18 @@ __global__ void __launch_bounds__(NWARPS * 32)
         const int c = 2 * kk + (mi & 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(sK + (c >> 3) * kHalfBytes + swz(key, c & 7), b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qa[kk], b0, b1);
-        mma_bf16_16816(s[1], qa[kk], b2, b3);
+        if (kk & 1) {
+          mma_bf16_16816(sx[0], qa[kk], b0, b1);
+          mma_bf16_16816(sx[1], qa[kk], b2, b3);
+        } else {
+          mma_bf16_16816(s[0], qa[kk], b0, b1);
+          mma_bf16_16816(s[1], qa[kk], b2, b3);
+        }
       }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[n][e] += sx[n][e];
     }
     // ---- mask, online softmax ----------------------------------------------------
     const bool need_mask = key0 + kBlock > lim_min;
@@ -392,6 +423,7 @@ __global__ void varlen_fixup_kernel(const int* __restrict__ desc, const float* _
                                     const int32_t* __restrict__ cu_seqlens_q, int num_workers,
                                     int Hq, int G, int QT, uint16_t* __restrict__ out,
                                     float* __restrict__ lse) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= num_workers) return;
@@ -599,11 +631,15 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   a.part_o = reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  paged_varlen_kernel<kWarps, kStages><<<g.grid, kWarps * 32, g.smem, st>>>(tmk, tmv, a);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_dependent(paged_varlen_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
+                       g.smem, st, tmk, tmv, a) != cudaSuccess)
+    return PA_ERR_CUDA;
   const int wpb = 8;
-  varlen_fixup_kernel<<<(g.workers + wpb - 1) / wpb, wpb * 32, 0, st>>>(
-      a.desc, a.part_o, a.part_lse, cu_seqlens_q, g.workers, a.Hq, a.G, a.QT, out, lse);
+  if (launch_dependent(varlen_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32), 0,
+                       st, (const int*)a.desc, (const float*)a.part_o, (const float*)a.part_lse,
+                       cu_seqlens_q, g.workers, a.Hq, a.G, a.QT, (uint16_t*)out,
+                       lse) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -129,3 +129,31 @@ def test_workspace_too_small_is_rejected():
         B.pa_decode(db.q, db.kc, db.vc, db.block_tables, db.context_lens, w.scale, out,
                     num_splits=0, workspace=small)
     assert e.value.status == B.PA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("case", ["tiny", "engine", "ragged_small"])
+def test_append_decode_equals_two_calls(case):
+    """pa_append_decode (write + decode in one call, the decode's preparation
+    overlapping the write) gives the same pool bytes as pa_reshape_and_cache
+    and the same results as pa_decode."""
+    name, sizes = CASES[case]
+    w = W.make(name, seed=20, **sizes)
+    ref = DeviceBatch(w)                  # history + new tokens written
+    ref_out, ref_lse = ref.decode(0)
+    fused = DeviceBatch(w, write_new=False)  # history only
+    out = torch.empty_like(fused.q)
+    lse = torch.empty(fused.q.shape[:2], dtype=torch.float32, device=fused.dev)
+    sh = B.shape_of(fused.q, fused.kc, fused.block_tables)
+    ws = B.workspace(B.pa_decode_workspace_size(sh, 0), fused.dev)
+    for _ in range(2):
+        B.pa_append_decode(fused.k_new, fused.v_new, fused.slot_new, fused.q, fused.kc, fused.vc,
+                           fused.block_tables, fused.context_lens, w.scale, out, lse,
+                           workspace=ws)
+        torch.cuda.synchronize()
+        assert B.pa_debug_read_error() == 0
+        assert torch.equal(fused.kc.view(torch.int16), ref.kc.view(torch.int16))
+        assert torch.equal(fused.vc.view(torch.int16), ref.vc.view(torch.int16))
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse, ref_lse)
+    ro, rl = oracle_attention(w)
+    assert_attention_close(out, lse, ro, rl, what=f"append/{case}")
