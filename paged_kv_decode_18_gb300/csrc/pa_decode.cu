@@ -37,7 +37,6 @@ namespace {
 constexpr int kG = 2;                          // query heads per KV head (built)
 constexpr int kQBytes = kG * kHeadDim * 2;     // 512
 constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
-constexpr int kDescInts = 8;
 
 template <int NSTAGE>
 struct WarpLayout {
@@ -64,7 +63,6 @@ struct DecodeArgs {
   int num_workers;  // kBalanced: warps launched
   float* part_o;    // kBalanced: [NW*2][G][D]; kFixed: [S][Hq][P][D]
   float* part_lse;  // kBalanced: [NW*2][G];    kFixed: [S][Hq][P]
-  int* desc;        // kBalanced: [NW][kDescInts]
   int early;        // 1: plan and table reads may run before the previous grid ends
 };
 
@@ -107,9 +105,9 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   // This grid is launched as a programmatic dependent of the previous one on
   // the stream. By default it waits for that grid right here, before reading
   // anything. With `early` (used only behind this library's own cache-write
-  // kernel, which writes nothing but the pool) the plan, the block-table
-  // window and the merge descriptors are prepared first and the wait sits
-  // just before the first copy out of the pool.
+  // kernel, which writes nothing but the pool) the plan and the block-table
+  // window are prepared first and the wait sits just before the first copy
+  // out of the pool.
   if (!a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   PlanInputs in;
   in.context_lens = a.context_lens;
@@ -146,8 +144,8 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   const int nw = min(a.num_workers, W);
   if (a.mode == kBalanced) {
     if (w < nw) {
-      R0 = (int)((int64_t)w * W / nw);
-      R1 = (int)((int64_t)(w + 1) * W / nw);
+      R0 = range_start(w, W, nw);
+      R1 = range_start(w + 1, W, nw);
     }
   } else {
     const int PS = a.num_splits;
@@ -176,10 +174,7 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     R0 = P.pair_off[pr] + h * nt + b0;
     R1 = R0 + (b1 - b0);
   }
-  if (R0 >= R1) {
-    if (a.mode == kBalanced && w < a.num_workers && lane == 0) a.desc[(size_t)w * kDescInts] = -1;
-    return;
-  }
+  if (R0 >= R1) return;
 
   const int grp = lane >> 3;   // tokens 4*grp .. 4*grp+3 of a tile
   const int c8 = lane & 7;     // dims 16*c8 .. 16*c8+15
@@ -189,9 +184,10 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   TilePos pp = locate(P, S, Hkv, R0);
   int pidx = R0;
   int wbase = R0;
+  // block id of flat tile idx; tiles of a window lie a few pairs past pp
   auto load_phys = [&](int idx) -> int {
     if (idx >= R1) return 0;
-    const TilePos t = locate(P, S, Hkv, idx);
+    const TilePos t = locate_from(P, Hkv, pp, idx);
     return a.block_tables[(size_t)t.s * a.max_blocks + t.b];
   };
   int phys_cur = load_phys(wbase + lane);
@@ -227,23 +223,6 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
 
   if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
-
-  if (a.mode == kBalanced && lane == 0) {
-    // Does this worker own the merge of the segment its range starts in?
-    int d[5] = {-1, 0, 0, 0, 0};
-    const TilePos t = locate(P, S, Hkv, R0);
-    const int A = R0 - t.b;  // flat start of the segment
-    const int R0prev = w > 0 ? (int)((int64_t)(w - 1) * W / nw) : 0;
-    if (t.b > 0 && A >= R0prev) {
-      const int B = A + t.nt;
-      d[0] = t.s;
-      d[1] = t.h;
-      d[2] = (int)(((int64_t)B * nw - 1) / W);  // worker holding the last tile
-      d[3] = (A == R0prev) ? 0 : 1;              // slot of worker w-1's piece
-    }
-    int* dd = a.desc + (size_t)w * kDescInts;
-    for (int i = 0; i < 5; ++i) dd[i] = d[i];
-  }
 
   // ---- consumer -------------------------------------------------------------
   // Lane (grp, c8) holds dims 16*c8..16*c8+15 of tokens 4*grp..4*grp+3 for
@@ -433,71 +412,80 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
 }
 
 // Merge the pieces of every (sequence, KV head) that the balanced ranges cut.
-// One warp per worker boundary; the owner recorded in desc[w] merges the
-// pieces held by workers w-1 .. last. Lane i reads piece i's lse values, so
-// the maxima and sums take one round of loads and a few shuffles; the partial
-// vectors are then loaded several pieces at a time. Launched as a dependent
-// grid: it may start while the decode kernel drains and waits for it here.
+// One warp per worker boundary. Launched as a dependent grid: while the decode
+// grid still runs, each CTA rebuilds the same plan from context_lens (which
+// the decode grid does not write) and each warp works out which segment it
+// must merge; only then does it wait for the decode grid, so after the decode
+// ends a single round of loads remains. Lane i reads piece i's lse values;
+// the partial vectors of a round are loaded together.
 __global__ void __launch_bounds__(256)
-    decode_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
-                        const float* __restrict__ part_lse, int num_workers, int Hq,
-                        uint16_t* __restrict__ out, float* __restrict__ lse) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+    decode_fixup_kernel(const int32_t* __restrict__ context_lens, int S, int Hkv, int max_blocks,
+                        int num_workers, const float* __restrict__ part_o,
+                        const float* __restrict__ part_lse, int Hq, uint16_t* __restrict__ out,
+                        float* __restrict__ lse) {
+  extern __shared__ __align__(16) int fx_smem[];
+  PlanSmem P;
+  P.pair_off = fx_smem;
+  P.seq_pair = P.pair_off + (S + 1);
+  P.ctx = P.seq_pair + (S + 1);
+  P.qstart = P.ctx + S;
+  PlanInputs in;
+  in.context_lens = context_lens;
+  in.cu_seqlens_q = nullptr;
+  in.S = S;
+  in.Hkv = Hkv;
+  in.max_ctx = max_blocks * kBlock;
+  in.qtile = 1;
+  in.causal = 1;
+  in.npairs_cap = S;
+  in.num_q_rows = S;
+  build_plan(in, P, nullptr);
+  const int W = P.total;
+  const int nw = min(num_workers, W);
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (w >= num_workers) return;
-  const int* d = desc + (size_t)w * kDescInts;
-  const int s = d[0];
-  if (s < 0) return;
-  const int h = d[1], last = d[2], slot_prev = d[3];
+  const MergeJob job = merge_job(P, S, Hkv, w, W, nw);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!job.valid) return;
+  const int s = job.s, h = job.h, last = job.last, slot_prev = job.slot_prev;
   const int npieces = last - w + 2;  // workers w-1 .. last
   float4 acc[kG];
   for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float LSE[kG];
-  // pass 1: log-sum-exp over all pieces (32 pieces per round)
+  // each round handles 32 pieces: lane i holds piece i's lse values while the
+  // partial vectors of the round are loaded at the same time
   float mx[kG] = {neg_inf(), neg_inf()}, sum[kG] = {0.f, 0.f};
   for (int i0 = 0; i0 < npieces; i0 += 32) {
-    const int i = i0 + lane;
+    const int n = min(32, npieces - i0);
     float li[kG] = {neg_inf(), neg_inf()};
-    if (i < npieces) {
-      const size_t slot = (size_t)(w - 1 + i) * 2 + (i == 0 ? slot_prev : 0);
-      const float2 v = *reinterpret_cast<const float2*>(part_lse + slot * kG);
+    if (lane < n) {
+      const float2 v = *reinterpret_cast<const float2*>(part_lse + ((size_t)(w - 1 + i0 + lane) * 2 + (i0 + lane == 0 ? slot_prev : 0)) * kG);
       li[0] = v.x;
       li[1] = v.y;
     }
+    float m[kG], e[kG];
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
-      float m = li[g];
+      m[g] = li[g];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      const float mnew = fmaxf(mx[g], m);
-      float e = ex2((li[g] - mnew) * kLog2e);
+      for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(kFull, m[g], o));
+      m[g] = fmaxf(m[g], mx[g]);
+      // rescale what earlier rounds accumulated to the new maximum
+      const float r = ex2((mx[g] - m[g]) * kLog2e);
+      sum[g] *= r;
+      acc[g].x *= r; acc[g].y *= r; acc[g].z *= r; acc[g].w *= r;
+      e[g] = ex2((li[g] - m[g]) * kLog2e);  // unnormalised weight of piece lane
+      float t = e[g];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(kFull, e, o);
-      sum[g] = sum[g] * ex2((mx[g] - mnew) * kLog2e) + e;
-      mx[g] = mnew;
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+      sum[g] += t;
+      mx[g] = m[g];
     }
-  }
-#pragma unroll
-  for (int g = 0; g < kG; ++g) LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
-  // pass 2: weighted sum of the partial outputs
-  for (int i0 = 0; i0 < npieces; i0 += 32) {
-    const int i = i0 + lane;
-    float wl[kG] = {0.f, 0.f};
-    if (i < npieces) {
-      const size_t slot = (size_t)(w - 1 + i) * 2 + (i == 0 ? slot_prev : 0);
-      const float2 v = *reinterpret_cast<const float2*>(part_lse + slot * kG);
-      wl[0] = ex2((v.x - LSE[0]) * kLog2e);
-      wl[1] = ex2((v.y - LSE[1]) * kLog2e);
-    }
-    const int n = min(32, npieces - i0);
 #pragma unroll 4
     for (int j = 0; j < n; ++j) {
-      const int ii = i0 + j;
-      const size_t slot = (size_t)(w - 1 + ii) * 2 + (ii == 0 ? slot_prev : 0);
+      const size_t slot = (size_t)(w - 1 + i0 + j) * 2 + (i0 + j == 0 ? slot_prev : 0);
 #pragma unroll
       for (int g = 0; g < kG; ++g) {
-        const float wt = __shfl_sync(kFull, wl[g], j);
+        const float wt = __shfl_sync(kFull, e[g], j);
         const float4 o =
             *reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4);
         acc[g].x = fmaf(wt, o.x, acc[g].x);
@@ -506,6 +494,13 @@ __global__ void __launch_bounds__(256)
         acc[g].w = fmaf(wt, o.w, acc[g].w);
       }
     }
+  }
+  float LSE[kG];
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
+    const float inv = 1.f / sum[g];
+    acc[g].x *= inv; acc[g].y *= inv; acc[g].z *= inv; acc[g].w *= inv;
   }
 #pragma unroll
   for (int g = 0; g < kG; ++g) {
@@ -569,8 +564,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part_o,
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kWarps = 6;
+constexpr int kStages = 2;
 
 struct DecodeGeometry {
   int mode = kBalanced;
@@ -578,6 +573,7 @@ struct DecodeGeometry {
   int grid = 0;
   int workers = 0;
   size_t smem = 0;
+  size_t fixup_smem = 0;
   size_t ws_desc = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
 };
 
@@ -606,7 +602,15 @@ int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
     g->mode = kBalanced;
     g->grid = dev.num_sms * per_sm;
     g->workers = g->grid * kWarps;
-    g->ws_desc = round_up(sizeof(int) * kDescInts * (size_t)g->workers, 256);
+    g->fixup_smem = plan_smem_bytes(S);
+    if (g->fixup_smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (g->fixup_smem > 48 * 1024 &&
+          cudaFuncSetAttribute(decode_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)g->fixup_smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    }
     g->ws_lse = round_up(sizeof(float) * 2 * kG * (size_t)g->workers, 256);
     g->ws_o = round_up(sizeof(float) * 2 * kG * kHeadDim * (size_t)g->workers, 256);
   } else {
@@ -704,7 +708,6 @@ int decode_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
   a.num_workers = g.workers;
   a.early = early;
   char* ws = static_cast<char*>(workspace);
-  a.desc = g.ws_desc ? reinterpret_cast<int*>(ws) : nullptr;
   a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
   a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
 
@@ -715,9 +718,9 @@ int decode_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
   if (g.mode == kBalanced) {
     // the merge grid may be scheduled while the decode grid drains; it waits
     // for the decode grid's completion before reading
-    if (launch_dependent(decode_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32), 0,
-                         st, (const int*)a.desc, (const float*)a.part_o,
-                         (const float*)a.part_lse, g.workers, a.Hq, (uint16_t*)out,
+    if (launch_dependent(decode_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32),
+                         g.fixup_smem, st, context_lens, a.S, a.Hkv, a.max_blocks, g.workers,
+                         (const float*)a.part_o, (const float*)a.part_lse, a.Hq, (uint16_t*)out,
                          lse) != cudaSuccess)
       return PA_ERR_CUDA;
   } else if (g.P > 1) {

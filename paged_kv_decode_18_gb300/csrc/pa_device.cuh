@@ -347,6 +347,57 @@ __device__ __forceinline__ TilePos locate(const PlanSmem& P, int S, int Hkv, int
   return t;
 }
 
+// Position of flat tile idx >= from's index, found by scanning forward from
+// `from` (a nearby position, usually the same or the next few pairs), which
+// is much cheaper than a binary search when idx is close.
+__device__ __forceinline__ TilePos locate_from(const PlanSmem& P, int Hkv, const TilePos& from,
+                                               int idx) {
+  TilePos t = from;
+  while (P.pair_off[t.p + 1] <= idx) ++t.p;
+  while (P.seq_pair[t.s + 1] <= t.p) ++t.s;
+  t.qt = t.p - P.seq_pair[t.s];
+  t.nt = (P.pair_off[t.p + 1] - P.pair_off[t.p]) / Hkv;
+  const int local = idx - P.pair_off[t.p];
+  t.h = local / t.nt;
+  t.b = local - t.h * t.nt;
+  return t;
+}
+
+// Start of worker w's range when W flat tiles are cut into nw equal
+// contiguous ranges: floor(w * W / nw).
+__device__ __forceinline__ int range_start(int w, int W, int nw) {
+  return (int)(((long long)w * W) / nw);
+}
+
+// The merge a worker boundary owns. A segment (pair, kv head) cut by range
+// boundaries is merged by the first boundary inside it: boundary w owns the
+// segment containing tile range_start(w) when that segment began inside worker
+// w-1's range. Its pieces are held by workers w-1 .. last: worker w-1 in slot
+// slot_prev (0 if the segment starts exactly at w-1's range start, else 1),
+// every later worker in slot 0.
+struct MergeJob {
+  bool valid;
+  int s, qt, h, last, slot_prev;
+};
+
+__device__ inline MergeJob merge_job(const PlanSmem& P, int S, int Hkv, int w, int W, int nw) {
+  MergeJob j;
+  j.valid = false;
+  if (w <= 0 || w >= nw) return j;
+  const int R0 = range_start(w, W, nw);
+  const TilePos t = locate(P, S, Hkv, R0);
+  const int A = R0 - t.b;  // flat start of the segment
+  const int R0prev = range_start(w - 1, W, nw);
+  if (t.b == 0 || A < R0prev) return j;
+  j.valid = true;
+  j.s = t.s;
+  j.qt = t.qt;
+  j.h = t.h;
+  j.last = (int)(((long long)(A + t.nt) * nw - 1) / W);  // worker holding the last tile
+  j.slot_prev = (A == R0prev) ? 0 : 1;
+  return j;
+}
+
 // Step a position to the next flat tile (only called while idx + 1 < total).
 __device__ __forceinline__ void advance(const PlanSmem& P, int S, int Hkv, TilePos& t) {
   if (++t.b < t.nt) return;

@@ -147,9 +147,10 @@ __global__ void __launch_bounds__(NWARPS * 32)
   // ---- producer --------------------------------------------------------------
   TilePos pp = locate(P, S, Hkv, R0);
   int pidx = R0, wbase = R0;
+  // block id of flat tile idx; tiles of a window lie a few pairs past pp
   auto load_phys = [&](int idx) -> int {
     if (idx >= R1) return 0;
-    const TilePos t = locate(P, S, Hkv, idx);
+    const TilePos t = locate_from(P, Hkv, pp, idx);
     return a.block_tables[(size_t)t.s * a.max_blocks + t.b];
   };
   int phys_cur = load_phys(wbase + lane);
