@@ -125,7 +125,11 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int W = P.total;
-  const int w = blockIdx.x * NWARPS + warp;
+  // Balanced ranges are dealt out transposed (range w = warp * gridDim.x + CTA):
+  // neighbouring ranges -- often the same kind of work -- land on different
+  // CTAs and SMs, so each SM gets a mix. Fixed splits keep the plain order.
+  const int w = a.mode == kBalanced ? warp * (int)gridDim.x + (int)blockIdx.x
+                                    : (int)blockIdx.x * NWARPS + warp;
 
   // Sequences with an empty context: out = 0, lse = -inf (balanced mode owns
   // them in CTA 0; fixed mode handles them through its empty partials).

@@ -18,8 +18,9 @@
 // in, fp32 accumulate) in tiles of 16 rows = (16/G) query tokens x G query
 // heads of one KV head against 16-key blocks:
 //   * K/V tiles arrive by 2-D TMA (cp.async.bulk.tensor) with the 128-byte
-//     swizzle, so ldmatrix reads them without bank conflicts; the Q rows of a
-//     tile arrive by 1-D bulk copies when a new (sequence, query tile) starts;
+//     swizzle, so ldmatrix reads them without bank conflicts; each warp loads
+//     the Q fragments of a (sequence, query tile) straight into registers when
+//     it starts one (a stage is only the 8 KB K/V tile);
 //   * one warp is one worker with a private ring of stages and a contiguous
 //     range of the batch's (sequence, query tile, KV head, block) tiles -- the
 //     same equal-range balancing as decode, so verify sequences, prefill
@@ -36,8 +37,7 @@ namespace {
 
 constexpr int kRows = 16;                      // rows of one query tile
 constexpr int kHalfBytes = kBlock * 128;       // 16 rows x 128 B (64 dims), swizzled
-constexpr int kQSlotBytes = kRows * kHeadDim * 2;  // 4 KB
-constexpr int kStageBytes = 4 * kHalfBytes + kQSlotBytes;  // K0 K1 V0 V1 Q = 12 KB
+constexpr int kStageBytes = 4 * kHalfBytes;  // K0 K1 V0 V1 = 8 KB
 constexpr int kDescInts = 8;
 
 struct VarlenArgs {
@@ -118,7 +118,11 @@ __global__ void __launch_bounds__(NWARPS * 32)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int W = P.total;
-  const int w = blockIdx.x * NWARPS + warp;
+  // ranges are dealt out transposed (range w = warp * gridDim.x + CTA):
+  // neighbouring ranges -- often the same kind of work (verify tiles streaming
+  // from HBM, or prefill tiles from L2) -- land on different CTAs and SMs, so
+  // each SM gets a mix
+  const int w = warp * (int)gridDim.x + (int)blockIdx.x;
   const int nw = min(a.num_workers, W);
   int R0 = 0, R1 = 0;
   if (w < nw) {
@@ -158,7 +162,6 @@ __global__ void __launch_bounds__(NWARPS * 32)
 
   auto issue = [&](int stage) {
     int phys = __shfl_sync(kFull, phys_cur, pidx - wbase);
-    const bool first = (pidx == R0) || (pp.b == 0);
     if (lane == 0) {
       if (phys < 0 || (int64_t)phys >= a.num_blocks) {
         flag_error(PA_DEVERR_BLOCK_RANGE);
@@ -166,23 +169,13 @@ __global__ void __launch_bounds__(NWARPS * 32)
       }
       unsigned char* st = wbuf + stage * kStageBytes;
       const uint32_t bar = smem_addr(&bars[stage]);
-      int nq = 0;
-      if (first) {
-        const int lq = P.qstart[pp.s + 1] - P.qstart[pp.s];
-        nq = min(QT, lq - pp.qt * QT);
-      }
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, 4 * kHalfBytes + nq * G * kHeadDim * 2);
+      mbar_arrive_expect_tx(bar, 4 * kHalfBytes);
       const int y = (int)(((int64_t)phys * Hkv + pp.h) * kBlock);
       tma_load_2d(smem_addr(st), &tmk, 0, y, bar);
       tma_load_2d(smem_addr(st + kHalfBytes), &tmk, 64, y, bar);
       tma_load_2d(smem_addr(st + 2 * kHalfBytes), &tmv, 0, y, bar);
       tma_load_2d(smem_addr(st + 3 * kHalfBytes), &tmv, 64, y, bar);
-      const int64_t row0 = (int64_t)P.qstart[pp.s] + (int64_t)pp.qt * QT;
-      for (int j = 0; j < nq; ++j)
-        bulk_copy_g2s(smem_addr(st + 4 * kHalfBytes + j * G * kHeadDim * 2),
-                      a.q + ((row0 + j) * Hq + (int64_t)pp.h * G) * kHeadDim,
-                      G * kHeadDim * 2, bar);
     }
     ++pidx;
     if (pidx < R1) advance(P, S, Hkv, pp);
@@ -219,25 +212,31 @@ __global__ void __launch_bounds__(NWARPS * 32)
     const uint32_t sK = smem_addr(st), sV = smem_addr(st + 2 * kHalfBytes);
     const bool first = (idx == R0) || (cp.b == 0);
     if (first) {
-      const uint32_t sQ = smem_addr(st + 4 * kHalfBytes);
       ctx = P.ctx[cp.s];
       lq = P.qstart[cp.s + 1] - P.qstart[cp.s];
-      // rows of query tokens past the sequence's last one are padding: zero
-      // them so they stay finite (they are never written out)
-      const int nq = min(QT, lq - cp.qt * QT);
-      if (nq < QT) {
-        unsigned char* qpad = st + 4 * kHalfBytes + nq * G * kHeadDim * 2;
-        const int chunks = (QT - nq) * G * kHeadDim * 2 / 16;
-        for (int i = lane; i < chunks; i += 32)
-          reinterpret_cast<uint4*>(qpad)[i] = make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-      }
-      const int mi = lane >> 3, rr = lane & 7;
-      const int qrow = (mi & 1) * 8 + rr;
+      // Q fragments straight from global memory: row r of the tile is token
+      // r / G, head r % G of this KV head. Rows past the sequence's last query
+      // token are padding and stay zero (never written out).
+      {
+        const uint32_t* qrow[2] = {nullptr, nullptr};
+        const int rws[2] = {r0, r1};
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        ldsm_x4(sQ + qrow * 256 + (2 * kk + (mi >> 1)) * 16, qa[kk][0], qa[kk][1], qa[kk][2],
-                qa[kk][3]);
+        for (int i = 0; i < 2; ++i) {
+          const int tok = cp.qt * QT + rws[i] / G;
+          if (tok < lq)
+            qrow[i] = reinterpret_cast<const uint32_t*>(
+                a.q + (((int64_t)P.qstart[cp.s] + tok) * Hq + (int64_t)cp.h * G + rws[i] % G) *
+                          kHeadDim);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int c = kk * 8 + quad;  // 32-bit word of dims kk*16 + 2*quad
+          qa[kk][0] = qrow[0] ? __ldg(qrow[0] + c) : 0u;
+          qa[kk][1] = qrow[1] ? __ldg(qrow[1] + c) : 0u;
+          qa[kk][2] = qrow[0] ? __ldg(qrow[0] + c + 4) : 0u;
+          qa[kk][3] = qrow[1] ? __ldg(qrow[1] + c + 4) : 0u;
+        }
+      }
 #pragma unroll
       for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
       m_r[0] = m_r[1] = neg_inf();
@@ -470,7 +469,7 @@ __global__ void varlen_fixup_kernel(const int* __restrict__ desc, const float* _
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-constexpr int kWarps = 4;
+constexpr int kWarps = 6;
 constexpr int kStages = 2;
 
 struct VarlenGeometry {
