@@ -395,7 +395,58 @@ def run_secondary(args, dev, B):
                                         "tokens_per_s": w.num_q_tokens / (ms / 1e3)}
         del kc, vc
         torch.cuda.empty_cache()
+    res.update(run_secondary_varlen(args, dev, B, peak))
     return res
+
+
+def attention_flops(w) -> int:
+    """Useful flops of one call: 4 * D per (query row, head, visible key)."""
+    n = 0
+    for c, l in zip(w.context_lens.tolist(), w.q_lens.tolist()):
+        n += sum(c - l + j + 1 for j in range(l)) if w.causal else l * c
+    return n * 4 * w.head_dim * w.num_q_heads
+
+
+def run_secondary_varlen(args, dev, B, peak):
+    """Verify + chunked-prefill call (tensor cores) on the mixed workload."""
+    from paged_kv_decode_18_gb300 import workloads as W
+
+    w = W.mixed(seed=args.seed)
+    kc, vc = w.empty_pool(dev)
+    B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
+    B.pa_reshape_and_cache(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), kc, vc)
+    q = w.q.to(dev)
+    bt, cl, cu = w.block_tables.to(dev), w.context_lens.to(dev), w.cu_seqlens_q.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    sh = B.shape_of(q, kc, bt)
+    ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, q.shape[0], w.max_q_len), dev)
+    fn = lambda: B.pa_decode_varlen(q, kc, vc, bt, cl, cu, w.max_q_len, w.scale, out, lse,  # noqa
+                                    causal=True, workspace=ws)
+    fn()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+        fn()
+    for _ in range(5):
+        g.replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(20)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(1_000_000)
+    for a, b in evs:
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / 2
+    alg = decode_algorithmic_bytes(w)
+    fl = attention_flops(w)
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"mixed_varlen": {"call_ms": round(ms, 5), "alg_bytes": alg, "achieved_gbs": round(gbs, 1),
+                             "frac_of_measured_peak": round(gbs / peak, 4), "useful_gflop": round(fl / 1e9, 3),
+                             "achieved_tflops": round(fl / (ms / 1e3) / 1e12, 1),
+                             "query_tokens_per_s": w.num_q_tokens / (ms / 1e3)}}
 
 
 # ---------------------------------------------------------------------------

@@ -269,6 +269,8 @@ __global__ void __launch_bounds__(NWARPS * 32)
                                   (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       __syncwarp();
+      // compiler barrier: the (volatile) ldmatrix reads below stay after the stores
+      asm volatile("" ::: "memory");
     }
 
     // ---- S = Q K^T (16 rows x 16 keys) -------------------------------------------

@@ -1,0 +1,100 @@
+"""The calls are stream-ordered, allocate nothing and never synchronise, so an
+engine can capture a whole decode step in a CUDA graph (S20, "The conflicts":
+CUDA graphs need fixed shapes) and replay it as its inputs change in place.
+Captured once, replayed on new contents, results match the oracle."""
+import pytest
+import torch
+
+from paged_kv_decode_18_gb300 import binding as B
+from paged_kv_decode_18_gb300 import build as libbuild
+from paged_kv_decode_18_gb300 import workloads as W
+from tests.gpu_util import DeviceBatch, assert_attention_close
+from tests.pools import oracle_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    libbuild.build()
+    B.load()
+
+
+def test_append_decode_graph_replays_on_new_inputs():
+    wa = W.ragged(seed=61, num_seqs=40, max_context=900)
+    wb = W.ragged(seed=62, num_seqs=40, max_context=900)
+    dev = torch.device("cuda:0")
+    # the same fixed-shape buffers serve both batches: pad tables / pools to the larger
+    nb = max(wa.num_blocks, wb.num_blocks)
+    mb = max(wa.max_blocks_per_seq, wb.max_blocks_per_seq)
+
+    def padded(w):
+        bt = torch.full((w.num_seqs, mb), -1, dtype=torch.int32)
+        bt[:, :w.max_blocks_per_seq] = w.block_tables
+        return bt
+
+    kc = torch.empty(nb, 8, 16, 128, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    q = torch.empty_like(wa.q, device=dev)
+    k_new = torch.empty_like(wa.k_new, device=dev)
+    v_new = torch.empty_like(wa.v_new, device=dev)
+    slots = torch.empty_like(wa.slot_new, device=dev)
+    bt = torch.empty(wa.num_seqs, mb, dtype=torch.int32, device=dev)
+    cl = torch.empty_like(wa.context_lens, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    sh = B.shape_of(q, kc, bt)
+    ws = B.workspace(B.pa_decode_workspace_size(sh, 0), dev)
+
+    def load(w):
+        kc.view(torch.int16).fill_(W.POOL_SENTINEL_BITS)
+        vc.view(torch.int16).fill_(W.POOL_SENTINEL_BITS)
+        B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
+        q.copy_(w.q)
+        k_new.copy_(w.k_new)
+        v_new.copy_(w.v_new)
+        slots.copy_(w.slot_new)
+        bt.copy_(padded(w))
+        cl.copy_(w.context_lens)
+
+    def step():
+        B.pa_append_decode(k_new, v_new, slots, q, kc, vc, bt, cl, wa.scale, out, lse,
+                           workspace=ws)
+
+    load(wa)
+    step()  # first call on the device before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for w in (wa, wb, wa):
+        load(w)
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.pa_debug_read_error() == 0
+        ref, ref_lse = oracle_attention(w)
+        assert_attention_close(out, lse, ref, ref_lse, what=f"graph replay seed {w.meta['seed']}")
+
+
+def test_varlen_graph_replay():
+    w = W.mixed(seed=63, num_verify=6, lo=40, hi=600, prefill_chunk=64, prefill_offsets=(0, 80))
+    db = DeviceBatch(w)
+    out = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.dev)
+    sh = B.shape_of(db.q, db.kc, db.block_tables)
+    ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, db.q.shape[0], w.max_q_len), db.dev)
+
+    def call():
+        B.pa_decode_varlen(db.q, db.kc, db.vc, db.block_tables, db.context_lens, db.cu_seqlens_q,
+                           w.max_q_len, w.scale, out, lse, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="varlen graph")
