@@ -195,8 +195,14 @@ int pa_decode_static_scratch(const pa_bf16* q, const pa_bf16* k_cache, const pa_
  * query window; "S20 - The Complete Engine", step 3 PROPOSE and step 5
  * verify) and chunked prefill (a chunk of queries at an offset whose earlier
  * tokens are already cached; course README, "chunked prefill"). QK^T and PV
- * run on the tensor cores in tiles of 16 rows = (16 / G) query tokens x G
- * query heads of one KV head.
+ * run on the tensor cores. Sequences with q_len < 32 (verify windows, short
+ * chunks) go through warp-level MMA tiles of 16 rows = (16 / G) query tokens x
+ * G query heads of one KV head; when max_q_len >= 32 and 128 % G == 0,
+ * sequences with q_len >= 32 go through a second kernel on the fifth-
+ * generation tensor cores (tcgen05, accumulators in tensor memory) in tiles
+ * of 128 rows x 128 keys. Both kernels are launched on `stream`, in order;
+ * the results do not depend on which kernel a sequence went through beyond
+ * floating-point rounding.
  *
  *   q             [num_q_tokens][Hq][D] bf16; sequence s owns rows
  *                 cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1

@@ -208,6 +208,9 @@ struct PlanInputs {
   int causal;
   int npairs_cap;
   int64_t num_q_rows;  // rows of q / out; every sequence's rows must lie inside
+  int key_tile = kBlock;       // keys per flat tile (a multiple of the block size)
+  int min_lq = 0;              // sequences whose q_len lies outside [min_lq, max_lq]
+  int max_lq = 0x7fffffff;     // belong to another kernel: no tiles here (not an error)
 };
 
 // Exclusive scan of n ints in shared memory, in place, by warp 0 of the CTA
@@ -237,9 +240,10 @@ __device__ inline int warp0_exclusive_scan(int* data, int n) {
 }
 
 // Number of key tiles query tile qt of sequence s needs (per KV head).
-__device__ __forceinline__ int pair_tiles(int c, int lq, int qt, int qtile, int causal) {
+__device__ __forceinline__ int pair_tiles(int c, int lq, int qt, int qtile, int causal,
+                                          int key_tile = kBlock) {
   int kv_end = causal ? (c - lq + min(qtile * (qt + 1), lq)) : c;
-  return (kv_end + kBlock - 1) / kBlock;
+  return (kv_end + key_tile - 1) / key_tile;
 }
 
 // Build the plan in shared memory. All threads of the CTA must call it; it
@@ -266,6 +270,7 @@ __device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scra
         flag_error(PA_DEVERR_QLEN_RANGE);
         lq = 0;  // the sequence produces no rows
       }
+      if (lq < in.min_lq || lq > in.max_lq) lq = 0;  // handled by another kernel
       P.qstart[s] = q0;
       P.seq_pair[s] = (lq + in.qtile - 1) / in.qtile;  // query tiles of s
       if (s == S - 1) P.qstart[S] = in.cu_seqlens_q[S];
@@ -299,8 +304,9 @@ __device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scra
       const int q0 = in.cu_seqlens_q[s];
       int lq = in.cu_seqlens_q[s + 1] - q0;
       if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) lq = 0;
+      if (lq < in.min_lq || lq > in.max_lq) lq = 0;
       for (int p = p0; p < p1; ++p)
-        P.pair_off[p] = in.Hkv * pair_tiles(c, lq, p - p0, in.qtile, in.causal);
+        P.pair_off[p] = in.Hkv * pair_tiles(c, lq, p - p0, in.qtile, in.causal, in.key_tile);
     }
     __syncthreads();
   }

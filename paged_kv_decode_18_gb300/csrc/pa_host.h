@@ -2,6 +2,8 @@
 // libpagedattn: status plumbing, shape checks, cached device properties.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -78,9 +80,38 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 bl
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// ---------------------------------------------------------------------------
+// tensor maps (pa_varlen.cu)
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// 2-D view of one pool array: [num_blocks * Hkv * 16 rows][128] bf16, boxes of
+// 16 rows x 64 dims, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows);
+
+// ---------------------------------------------------------------------------
+// tcgen05 prefill path (pa_prefill_tc.cu): sequences with q_len >= this go
+// there; the mma.sync varlen kernel takes the shorter ones (verify).
+// ---------------------------------------------------------------------------
+constexpr int kTcMinQLen = 32;
+
+struct PrefillTcGeometry {
+  bool enabled = false;
+  int grid = 0, workers = 0, npairs_cap = 0, QTb = 0;
+  size_t smem = 0, fixup_smem = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
+};
+
+int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
+                        PrefillTcGeometry* g);
+int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf16* k_cache,
+                      const pa_bf16* v_cache, const int32_t* block_tables,
+                      const int32_t* context_lens, const int32_t* cu_seqlens_q,
+                      int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
+                      const pa_shape* sh, void* workspace, cudaStream_t st);
+
 // Each TU that owns kernels exposes the reader of its device error word.
 unsigned take_error_word_cache(cudaStream_t stream, int* rc);
 unsigned take_error_word_decode(cudaStream_t stream, int* rc);
 unsigned take_error_word_varlen(cudaStream_t stream, int* rc);
+unsigned take_error_word_prefill(cudaStream_t stream, int* rc);
 
 }  // namespace pa

@@ -54,6 +54,7 @@ struct VarlenArgs {
   int causal;
   int npairs_cap;
   int num_workers;
+  int max_lq;       // longer sequences go to the tcgen05 prefill kernel
   float* part_o;    // [NW*2][16][D]
   float* part_lse;  // [NW*2][16]
   int* desc;        // [NW][kDescInts]
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(NWARPS * 32)
   in.causal = a.causal;
   in.npairs_cap = a.npairs_cap;
   in.num_q_rows = a.num_q_tokens;
+  in.max_lq = a.max_lq;
   build_plan(in, P, scratch);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -526,10 +528,10 @@ int check_varlen_args(const pa_shape* shape, int64_t num_q_tokens, int max_q_len
   return PA_OK;
 }
 
-using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+}  // namespace
 
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
     void* p = nullptr;
@@ -537,15 +539,13 @@ EncodeFn encode_fn() {
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
   return fn;
 }
 
-// 2-D view of one pool array: [num_blocks * Hkv * 16 rows][128] bf16, boxes of
-// 16 rows x 64 dims, 128-byte swizzle.
 bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
-  EncodeFn fn = encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
@@ -555,8 +555,6 @@ bool make_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 unsigned take_error_word_varlen(cudaStream_t stream, int* rc) {
   unsigned v = 0, zero = 0;
@@ -579,7 +577,9 @@ extern "C" size_t pa_decode_varlen_workspace_size(const pa_shape* shape, int64_t
   if (shape->num_seqs == 0 || num_q_tokens == 0) return 0;
   VarlenGeometry g;
   if (varlen_geometry(shape, num_q_tokens, max_q_len, &g) != PA_OK) return 0;
-  return g.ws_bytes;
+  PrefillTcGeometry tg;
+  if (prefill_tc_geometry(shape, num_q_tokens, max_q_len, &tg) != PA_OK) return 0;
+  return g.ws_bytes + tg.ws_bytes;
 }
 
 extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
@@ -601,7 +601,10 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   VarlenGeometry g;
   rc = varlen_geometry(shape, num_q_tokens, max_q_len, &g);
   if (rc != PA_OK) return rc;
-  if (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256))
+  PrefillTcGeometry tg;
+  rc = prefill_tc_geometry(shape, num_q_tokens, max_q_len, &tg);
+  if (rc != PA_OK) return rc;
+  if (!workspace || workspace_bytes < g.ws_bytes + tg.ws_bytes || !aligned(workspace, 256))
     return PA_ERR_WORKSPACE;
   const int64_t rows = shape->num_blocks * shape->num_kv_heads * kBlock;
   CUtensorMap tmk, tmv;
@@ -627,12 +630,19 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   a.causal = causal ? 1 : 0;
   a.npairs_cap = g.npairs_cap;
   a.num_workers = g.workers;
+  a.max_lq = tg.enabled ? kTcMinQLen - 1 : 0x7fffffff;
   char* ws = static_cast<char*>(workspace);
   a.desc = reinterpret_cast<int*>(ws);
   a.part_lse = reinterpret_cast<float*>(ws + g.ws_desc);
   a.part_o = reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (tg.enabled) {
+    // sequences with long query chunks (prefill): tcgen05 tiles of 128 rows
+    rc = launch_prefill_tc(tg, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
+                           num_q_tokens, causal, scale, out, lse, shape, ws + g.ws_bytes, st);
+    if (rc != PA_OK) return rc;
+  }
   if (launch_dependent(paged_varlen_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
                        g.smem, st, tmk, tmv, a) != cudaSuccess)
     return PA_ERR_CUDA;

@@ -74,3 +74,46 @@ def test_zero_q_len_sequences_produce_no_rows():
     assert B.pa_debug_read_error() == 0
     ref, ref_lse = oracle_attention(w)
     assert_attention_close(out, lse, ref, ref_lse, what="zero q_len")
+
+
+# Sequences with q_len >= 32 run on the tcgen05 prefill tile (128 query rows
+# per KV head); shorter ones on the mma.sync tile. These cases cover the long
+# path with every group size, ragged context tails, and both paths at once.
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (8, 8), (16, 4), (32, 4)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_tiles_group_sizes(hq, hkv, causal):
+    # q_len 32..300 at offsets that leave ragged 16- and 128-key tails
+    w = W.build("tc", 31, [45, 300, 777, 130, 1029], [32, 300, 129, 65, 40], pool_factor=1.2,
+                num_q_heads=hq, num_kv_heads=hkv, causal=causal)
+    db = DeviceBatch(w)
+    out, lse = db.varlen(causal=causal)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what=f"tc G={hq // hkv} causal={causal}")
+
+
+def test_prefill_and_verify_in_one_call():
+    w = W.build("both", 32, [300, 17, 2000, 64, 600, 5], [200, 5, 512, 33, 31, 5],
+                pool_factor=1.15)
+    db = DeviceBatch(w)
+    out, lse = db.varlen()
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="tc + mma paths")
+
+
+def test_prefill_segment_cut_into_many_pieces():
+    # one query tile per KV head over 8192 keys: 8 segments of 64 key tiles
+    # spread over every CTA, so each segment is merged from ~20 pieces
+    w = W.build("cut", 33, [8192, 40], [64, 40], pool_factor=1.1)
+    db = DeviceBatch(w)
+    out, lse = db.varlen()
+    out_nl, _ = db.varlen(with_lse=False)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="many pieces")
+    assert torch.equal(out, out_nl)
