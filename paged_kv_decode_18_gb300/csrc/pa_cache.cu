@@ -19,8 +19,11 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
                                          const int64_t* __restrict__ slots, int64_t total_chunks,
                                          int Hkv, int64_t num_slots, uint4* __restrict__ k_cache,
                                          uint4* __restrict__ v_cache) {
-  // a dependent grid queued behind this one (decode in pa_append_decode) may
-  // start its own preparation now; it waits for this grid before reading the pool
+  // launched as a programmatic dependent: wait for the previous grid (which may
+  // produce k, v or the slots), then let a dependent grid queued behind this
+  // one (decode in pa_append_decode) start its own preparation; that grid
+  // reads only call inputs before it waits for this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= total_chunks) return;
@@ -73,10 +76,12 @@ extern "C" int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v,
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 0x7fffffff) return PA_ERR_ARG;
-  reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), slot_mapping, total,
-      shape->num_kv_heads, shape->num_blocks * shape->block_size,
-      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache));
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_dependent(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                       static_cast<cudaStream_t>(stream), reinterpret_cast<const uint4*>(k),
+                       reinterpret_cast<const uint4*>(v), slot_mapping, total,
+                       shape->num_kv_heads, shape->num_blocks * shape->block_size,
+                       reinterpret_cast<uint4*>(k_cache),
+                       reinterpret_cast<uint4*>(v_cache)) != cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }

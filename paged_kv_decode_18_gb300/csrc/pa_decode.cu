@@ -427,6 +427,9 @@ __global__ void __launch_bounds__(256)
                         int num_workers, const float* __restrict__ part_o,
                         const float* __restrict__ part_lse, int Hq, uint16_t* __restrict__ out,
                         float* __restrict__ lse) {
+  // the next grid in the stream may start its own preparation now; it waits
+  // for this grid before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(16) int fx_smem[];
   PlanSmem P;
   P.pair_off = fx_smem;

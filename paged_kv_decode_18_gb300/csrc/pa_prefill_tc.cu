@@ -41,23 +41,23 @@ constexpr int kKeysT = 128;                 // keys per tile (N of S, K of PV)
 constexpr int kBlocksT = kKeysT / kBlock;   // pool blocks per key tile
 constexpr int kHalfT = kRowsT * 128;        // one 64-column half of a 128-row bf16 operand
 constexpr int kOpBytes = 2 * kHalfT;        // a 128 x 128 bf16 operand
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kOpBytes;    // stage s: K at kOffKV + s * 2 * kOpBytes, V after it
-constexpr int kOffP = kOffKV + 2 * 2 * kOpBytes;
-constexpr int kOffBar = kOffP + kOpBytes;
-constexpr int kNumBars = 18;
+constexpr int kOffQ = 0;                   // two query-tile buffers
+constexpr int kOffKV = kOffQ + 2 * kOpBytes;  // stage s: K at kOffKV + s * 2 * kOpBytes, V after it
+constexpr int kOffBar = kOffKV + 2 * 2 * kOpBytes;
+constexpr int kNumBars = 20;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffLx = kOffBar + 256;       // [2 pieces][2 halves][128 rows] x (m, l)
 constexpr int kOffPlan = kOffLx + 2 * 2 * kRowsT * 8;
-constexpr int kSoftmaxWarps = 8;            // two per SM sub-partition
-constexpr int kThreadsT = 64 + kSoftmaxWarps * 32;
+constexpr int kSoftmaxWarps = 8;            // warps 2-9, two per SM sub-partition
+constexpr int kVWarp = 2 + kSoftmaxWarps;   // the V producer
+constexpr int kThreadsT = 96 + kSoftmaxWarps * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;             // S buffers at columns 0 and 128; O halves at 256, 384
+constexpr uint32_t kColO = 256;             // S/P buffers at columns 0 and 128; O halves at 256, 384
 constexpr float kRescaleLog2 = 8.f;         // lazy O rescale threshold (log2 units)
 
 enum : int {
-  B_QFULL = 0, B_QEMPTY,
+  B_QFULL = 0, B_QFULL1, B_QEMPTY, B_QEMPTY1,
   B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1,
   B_VFULL, B_VFULL1, B_VEMPTY, B_VEMPTY1,
   B_SFULL, B_SFULL1, B_SFREE, B_SFREE1,
@@ -109,6 +109,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// A (M x K, K-major) read from tensor memory at column a_tmem, B from shared memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   plan_view(smem + kOffPlan, a, P);
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool all = i == B_SFREE || i == B_SFREE1 || i == B_PFULL || i == B_LX || i == B_LX1;
+      const bool all = i == B_PFULL || i == B_LX || i == B_LX1;
       mbar_init(bar(i), all ? (uint32_t)(kSoftmaxWarps * 32) : 1u);
     }
     *abort_flag = 0;
@@ -287,8 +296,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     return true;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------------ producers
+    // warp 0 loads the query tiles and K, warp kVWarp loads V: each stage's K
+    // is refilled as soon as its S is done, without queueing behind the V of
+    // the previous tile (which waits for that tile's PV)
+    const bool is_k = warp == 0;
     TilePos t = locate(P, S, Hkv, R0);
     auto nblocks_of = [&](const TilePos& tp) {
       const int nb_seq = (P.ctx[tp.s] + kBlock - 1) / kBlock;
@@ -299,17 +312,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                  ? a.block_tables[(size_t)tp.s * a.max_blocks + tp.b * kBlocksT + lane]
                  : 0;
     };
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    const int b_full = is_k ? B_KFULL : B_VFULL, b_empty = is_k ? B_KEMPTY : B_VEMPTY;
     int ids = fetch_ids(t);
     int qn = 0;
     for (int idx = R0, i = 0; idx < R1; ++idx, ++i) {
       const bool first = (idx == R0) || (t.b == 0);
-      if (first) {
-        if (qn > 0 && !wait(B_QEMPTY, (uint32_t)(qn - 1) & 1u)) break;
+      if (is_k && first) {
+        const int qs = qn & 1;
+        if (qn >= 2 && !wait(B_QEMPTY + qs, (uint32_t)((qn >> 1) - 1) & 1u)) break;
         if (lane == 0) {
           const int z = P.qstart[t.s] + t.qt * QTb;  // first query token of the tile
-          mbar_arrive_expect_tx(bar(B_QFULL), kOpBytes);
-          tma_load_3d(smem_addr(smem + kOffQ), &tmq, 0, t.h * G, z, bar(B_QFULL));
-          tma_load_3d(smem_addr(smem + kOffQ + kHalfT), &tmq, 64, t.h * G, z, bar(B_QFULL));
+          const uint32_t qd = smem_addr(smem + kOffQ + qs * kOpBytes);
+          mbar_arrive_expect_tx(bar(B_QFULL + qs), kOpBytes);
+          tma_load_3d(qd, &tmq, 0, t.h * G, z, bar(B_QFULL + qs));
+          tma_load_3d(qd + kHalfT, &tmq, 64, t.h * G, z, bar(B_QFULL + qs));
         }
         ++qn;
       }
@@ -322,27 +339,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         ids = fetch_ids(tn);
       }
       if (lane < nb && (my_id < 0 || (int64_t)my_id >= a.num_blocks)) {
-        flag_error(PA_DEVERR_BLOCK_RANGE);
+        if (is_k) flag_error(PA_DEVERR_BLOCK_RANGE);
         my_id = 0;
       }
       const int y = (int)(((int64_t)my_id * Hkv + t.h) * kBlock);
-      const uint32_t ph = (uint32_t)((i >> 1) - 1) & 1u;
-      // K of this tile: its stage is free once the S of tile i-2 is done
-      if (i >= 2 && !wait(B_KEMPTY + st, ph)) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_KFULL + st), (uint32_t)nb * (uint32_t)kTileBytes);
+      // the stage is free once the S (K) or the PV (V) of tile i-2 is done
+      if (i >= 2 && !wait(b_empty + st, (uint32_t)((i >> 1) - 1) & 1u)) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(b_full + st), (uint32_t)nb * (uint32_t)kTileBytes);
       __syncwarp();
-      unsigned char* kd = smem + kOffKV + st * 2 * kOpBytes + lane * (kBlock * 128);
+      const uint32_t d = smem_addr(smem + kOffKV + st * 2 * kOpBytes + (is_k ? 0 : kOpBytes) +
+                                   lane * (kBlock * 128));
       if (lane < nb) {
-        tma_load_2d(smem_addr(kd), &tmk, 0, y, bar(B_KFULL + st));
-        tma_load_2d(smem_addr(kd + kHalfT), &tmk, 64, y, bar(B_KFULL + st));
-      }
-      // V: free once the PV of tile i-2 is done
-      if (i >= 2 && !wait(B_VEMPTY + st, ph)) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_VFULL + st), (uint32_t)nb * (uint32_t)kTileBytes);
-      __syncwarp();
-      if (lane < nb) {
-        tma_load_2d(smem_addr(kd + kOpBytes), &tmv, 0, y, bar(B_VFULL + st));
-        tma_load_2d(smem_addr(kd + kOpBytes + kHalfT), &tmv, 64, y, bar(B_VFULL + st));
+        tma_load_2d(d, map, 0, y, bar(b_full + st));
+        tma_load_2d(d + kHalfT, map, 64, y, bar(b_full + st));
       }
       __syncwarp();
       if (idx + 1 < R1) advance(P, S, Hkv, t);
@@ -352,17 +361,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     if (lane == 0) {
       const uint32_t idS = f16_idesc(kRowsT, kKeysT, 0);
       const uint32_t idPV = f16_idesc(kRowsT, 128, 1);
-      const uint32_t sQ = smem_addr(smem + kOffQ), sP = smem_addr(smem + kOffP);
-      int qn = 0;
+      int qn = 0, qs = 0;  // query tiles seen; buffer of the current one
       auto issue_S = [&](int i, bool first) -> bool {
         if (first) {
-          if (!wait(B_QFULL, (uint32_t)qn & 1u)) return false;
+          qs = qn & 1;
+          if (!wait(B_QFULL + qs, (uint32_t)(qn >> 1) & 1u)) return false;
           ++qn;
         }
         const int st = i & 1;
         if (!wait(B_KFULL + st, (uint32_t)(i >> 1) & 1u)) return false;
+        // the S/P buffer is free once the PV that read P of tile i-2 is done
         if (i >= 2 && !wait(B_SFREE + st, (uint32_t)((i >> 1) - 1) & 1u)) return false;
         tc_fence_after();
+        const uint32_t sQ = smem_addr(smem + kOffQ + qs * kOpBytes);
         const uint32_t sK = smem_addr(smem + kOffKV + st * 2 * kOpBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // head_dim 128 = 8 steps of 16
@@ -376,7 +387,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       };
       TilePos t = locate(P, S, Hkv, R0);
       bool ok = issue_S(0, true);
-      if (ok && (R0 + 1 >= R1 || t.b == t.nt - 1)) tc_commit(bar(B_QEMPTY));
+      if (ok && (R0 + 1 >= R1 || t.b == t.nt - 1)) tc_commit(bar(B_QEMPTY + qs));
       for (int idx = R0, i = 0; ok && idx < R1; ++idx, ++i) {
         const bool first = (idx == R0) || (t.b == 0);
         if (idx + 1 < R1) {
@@ -387,7 +398,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             ok = false;
             break;
           }
-          if (idx + 2 >= R1 || tn.b == tn.nt - 1) tc_commit(bar(B_QEMPTY));
+          if (idx + 2 >= R1 || tn.b == tn.nt - 1) tc_commit(bar(B_QEMPTY + qs));
         }
         const int st = i & 1;
         if (!wait(B_PFULL, (uint32_t)i & 1u) || !wait(B_VFULL + st, (uint32_t)(i >> 1) & 1u)) {
@@ -396,16 +407,18 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         }
         tc_fence_after();
         const uint32_t sV = smem_addr(smem + kOffKV + st * 2 * kOpBytes + kOpBytes);
-        // O_hf += P[:, keys of half hf] V[keys of half hf, :]: one accumulator per key half
+        // O_hf += P[:, keys of half hf] V[keys of half hf, :]: one accumulator per
+        // key half; P (bf16 pairs) sits in columns st*128 + hf*64 .. +31 of TMEM
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc_mma(tmem + kColO + (uint32_t)hf * 128u,
-                   sw128_desc(sP + (uint32_t)hf * kHalfT + (uint32_t)k * 32u, 16, 1024),
-                   sw128_desc(sV + (uint32_t)(hf * 4 + k) * 2048u, kHalfT, 1024), idPV,
-                   (k > 0 || !first) ? 1u : 0u);
+            tc_mma_ts(tmem + kColO + (uint32_t)hf * 128u,
+                      tmem + (uint32_t)st * 128u + (uint32_t)hf * 64u + (uint32_t)k * 8u,
+                      sw128_desc(sV + (uint32_t)(hf * 4 + k) * 2048u, kHalfT, 1024), idPV,
+                      (k > 0 || !first) ? 1u : 0u);
         tc_commit(bar(B_VEMPTY + st));
+        tc_commit(bar(B_SFREE + st));
         tc_commit(bar(B_ODONE));
         if (idx + 1 < R1) advance(P, S, Hkv, t);
       }
@@ -421,14 +434,73 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const int r = q4 * 32 + lane;  // this thread's query row (= TMEM lane)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const uint32_t tO = tmem + lane_base + kColO;
-    const uint32_t sProw = smem_addr(smem + kOffP) + (uint32_t)hf * kHalfT + (uint32_t)r * 128u;
     float* lx = reinterpret_cast<float*>(smem + kOffLx);
     const float sc = a.scale_log2;
     TilePos t = locate(P, S, Hkv, R0);
     float m_ref = neg_inf(), l = 0.f;
     int lim = 0, c = 0, lq = 0, tok = 0, piece_b0 = 0, np = 0;
     bool valid = false, piece_first = true;
-    for (int idx = R0, i = 0; idx < R1; ++idx, ++i) {
+    // A finished piece's O stays in TMEM until the next tile's exponentials
+    // are done (its last PV completes meanwhile); then it is written out.
+    bool pend = false, pend_complete = false, pend_valid = false;
+    int pend_np = 0;
+    int64_t pend_orow = 0;
+    size_t pend_slot = 0;
+    float pend_m = 0.f, pend_l = 0.f;
+    auto flush = [&]() -> bool {
+      // merge the two key halves of the row: the partner's (m, l) from shared memory
+      if (!wait(B_LX + (pend_np & 1), (uint32_t)(pend_np >> 1) & 1u)) return false;
+      const float* other = lx + ((pend_np & 1) * 2 + (hf ^ 1)) * kRowsT * 2 + r * 2;
+      const float m_o = other[0], l_o = other[1];
+      const float M = fmaxf(pend_m, m_o);
+      const float a_me = pend_m == neg_inf() ? 0.f : ex2(pend_m - M);
+      const float a_o = m_o == neg_inf() ? 0.f : ex2(m_o - M);
+      const float lt = pend_l * a_me + l_o * a_o;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float c0 = (hf == 0 ? a_me : a_o) * inv, c1 = (hf == 0 ? a_o : a_me) * inv;
+      const float lse_v = lt > 0.f ? (M + lg2(lt)) * kLn2 : neg_inf();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int d0 = hf * 64 + cc * 32;  // output dims d0 .. d0+31
+        uint32_t u0[32], u1[32];
+        tmem_ld32_async(tO + (uint32_t)d0, u0);
+        tmem_ld32_async(tO + 128u + (uint32_t)d0, u1);
+        tmem_wait_ld(u0);
+        tmem_tie(u1);
+        float o[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          o[j] = fmaf(__uint_as_float(u0[j]), c0, __uint_as_float(u1[j]) * c1);
+        if (pend_complete) {
+          if (pend_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(a.out + pend_orow * kHeadDim + d0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(cvt_bf16x2(o[8 * q + 0], o[8 * q + 1]),
+                                  cvt_bf16x2(o[8 * q + 2], o[8 * q + 3]),
+                                  cvt_bf16x2(o[8 * q + 4], o[8 * q + 5]),
+                                  cvt_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+          }
+        } else {
+          float4* dst =
+              reinterpret_cast<float4*>(a.part_o + (pend_slot * kRowsT + r) * kHeadDim + d0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      if (hf == 0) {
+        if (pend_complete) {
+          if (pend_valid && a.lse) a.lse[pend_orow] = lse_v;
+        } else {
+          a.part_lse[pend_slot * kRowsT + r] = lse_v;
+        }
+      }
+      pend = false;
+      return true;
+    };
+    int i = 0;
+    for (int idx = R0; idx < R1; ++idx, ++i) {
       const bool first = (idx == R0) || (t.b == 0);
       const bool last = (idx == R1 - 1) || (t.b == t.nt - 1);
       if (first) {
@@ -451,8 +523,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       tmem_ld32_async(tS + 32u, v1);
       tmem_wait_ld(v0);
       tmem_tie(v1);
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE + sb));  // this S buffer may be overwritten now
 
       // scores in log2 units
       float2 x[32];
@@ -512,9 +582,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       }
       const float2 s01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
       l = fmaf(l, alpha, s01.x + s01.y);
-      // the previous PV must be done before P is replaced or O is rescaled
+      // the previous PV must be done before P is replaced, O is rescaled or the
+      // previous piece's O is read
       if (i > 0 && !wait(B_ODONE, (uint32_t)(i - 1) & 1u)) break;
       tc_fence_after();
+      if (pend && !flush()) break;
       if (rescale && !first) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -525,16 +597,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
           tmem_st32(ta, v);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      // P row r, keys of half hf: one 128-byte row of that half, 16-byte chunks swizzled
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t dst = sProw + (uint32_t)((ch ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[4 * ch]),
-                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                     : "memory");
-      }
+      // P row r, keys of half hf, over the S columns this thread has read
+      tmem_st32(tS, pk);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       // keys past the context may hold anything (even NaN): zero their V rows
       // so that P = 0 never meets them (thread (r, hf) clears half hf of key row r)
       const int key0 = t.b * kKeysT;
@@ -544,74 +610,32 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           *reinterpret_cast<uint4*>(vrow + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL));
 
       if (last) {
-        // merge the two key halves of row r: (m, l) through shared memory
+        // hand (m, l) of this half to the partner thread; O is written out
+        // during the next tile (or after the loop)
         float* mine = lx + ((np & 1) * 2 + hf) * kRowsT * 2 + r * 2;
-        float* other = lx + ((np & 1) * 2 + (hf ^ 1)) * kRowsT * 2 + r * 2;
         mine[0] = m_ref;
         mine[1] = l;
         mbar_arrive(bar(B_LX + (np & 1)));
-        if (!wait(B_LX + (np & 1), (uint32_t)(np >> 1) & 1u)) break;
-        ++np;
-        const float m_o = other[0], l_o = other[1];
-        const float M = fmaxf(m_ref, m_o);
-        const float a_me = m_ref == neg_inf() ? 0.f : ex2(m_ref - M);
-        const float a_o = m_o == neg_inf() ? 0.f : ex2(m_o - M);
-        const float lt = l * a_me + l_o * a_o;
-        const float a0 = hf == 0 ? a_me : a_o, a1 = hf == 0 ? a_o : a_me;
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float c0 = a0 * inv, c1 = a1 * inv;
-        const float lse_v = lt > 0.f ? (M + lg2(lt)) * kLn2 : neg_inf();
-        if (!wait(B_ODONE, (uint32_t)i & 1u)) break;
-        tc_fence_after();
-        const bool complete = (piece_b0 == 0) && (t.b == t.nt - 1);
-        const int g = r % G;
-        const int64_t orow =
-            ((int64_t)P.qstart[t.s] + tok) * a.Hq + (int64_t)t.h * G + g;
-        const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int d0 = hf * 64 + cc * 32;  // output dims d0 .. d0+31
-          uint32_t u0[32], u1[32];
-          tmem_ld32_async(tO + (uint32_t)d0, u0);
-          tmem_ld32_async(tO + 128u + (uint32_t)d0, u1);
-          tmem_wait_ld(u0);
-          tmem_tie(u1);
-          float o[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            o[j] = fmaf(__uint_as_float(u0[j]), c0, __uint_as_float(u1[j]) * c1);
-          if (complete) {
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kHeadDim + d0);
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(cvt_bf16x2(o[8 * q + 0], o[8 * q + 1]),
-                                    cvt_bf16x2(o[8 * q + 2], o[8 * q + 3]),
-                                    cvt_bf16x2(o[8 * q + 4], o[8 * q + 5]),
-                                    cvt_bf16x2(o[8 * q + 6], o[8 * q + 7]));
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * kRowsT + r) * kHeadDim + d0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          }
-        }
-        if (hf == 0) {
-          if (complete) {
-            if (valid && a.lse) a.lse[orow] = lse_v;
-          } else {
-            a.part_lse[slot * kRowsT + r] = lse_v;
-          }
-        }
+        pend = true;
+        pend_np = np++;
+        pend_m = m_ref;
+        pend_l = l;
+        pend_complete = (piece_b0 == 0) && (t.b == t.nt - 1);
+        pend_valid = valid;
+        pend_orow = ((int64_t)P.qstart[t.s] + tok) * a.Hq + (int64_t)t.h * G + r % G;
+        pend_slot = (size_t)w * 2 + (piece_first ? 0 : 1);
       }
       if (idx + 1 < R1) advance(P, S, Hkv, t);
+    }
+    if (pend && !*abort_flag && wait(B_ODONE, (uint32_t)(i - 1) & 1u)) {
+      tc_fence_after();
+      flush();
     }
   }
 
@@ -634,6 +658,9 @@ constexpr int kFixThreads = 256;
 
 __global__ void __launch_bounds__(kFixThreads)
     prefill_tc_fixup_kernel(const TcArgs a) {
+  // the next grid in the stream may start its own preparation now; it waits
+  // for this grid before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(16) unsigned char fx_smem[];
   PlanSmem P;
   plan_view(fx_smem, a, P);
@@ -657,31 +684,51 @@ __global__ void __launch_bounds__(kFixThreads)
   const int d0 = (lane & 7) * 16;
   const int tok = job.qt * a.QTb + r / a.G;
   if (tok >= lq) return;
-  float mx = neg_inf();
-  for (int i = 0; i < npieces; ++i) mx = fmaxf(mx, a.part_lse[slot_of(i) * kRowsT + r]);
-  float sum = 0.f;
-  for (int i = 0; i < npieces; ++i)
-    sum += mx == neg_inf() ? 0.f : ex2((a.part_lse[slot_of(i) * kRowsT + r] - mx) * kLog2e);
-  const float LSE = sum > 0.f ? mx + lg2(sum) * kLn2 : neg_inf();
+  // online merge over the pieces, four at a time with all their loads in flight
+  float m = neg_inf(), sum = 0.f;
   float acc[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-  for (int i = 0; i < npieces; ++i) {
-    const size_t sl = slot_of(i);
-    const float li = a.part_lse[sl * kRowsT + r];
-    const float wt = (sum > 0.f && li != neg_inf()) ? ex2((li - LSE) * kLog2e) : 0.f;
-    const float4* src = reinterpret_cast<const float4*>(a.part_o + (sl * kRowsT + r) * kHeadDim + d0);
-    float4 x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = src[u];
+  for (int i0 = 0; i0 < npieces; i0 += 4) {
+    float li[4];
+    float4 x[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      acc[4 * u + 0] = fmaf(wt, x[u].x, acc[4 * u + 0]);
-      acc[4 * u + 1] = fmaf(wt, x[u].y, acc[4 * u + 1]);
-      acc[4 * u + 2] = fmaf(wt, x[u].z, acc[4 * u + 2]);
-      acc[4 * u + 3] = fmaf(wt, x[u].w, acc[4 * u + 3]);
+      li[u] = neg_inf();
+      x[u][0] = x[u][1] = x[u][2] = x[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i0 + u < npieces) {
+        const size_t sl = slot_of(i0 + u);
+        li[u] = a.part_lse[sl * kRowsT + r];
+        const float4* src =
+            reinterpret_cast<const float4*>(a.part_o + (sl * kRowsT + r) * kHeadDim + d0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[u][k] = src[k];
+      }
     }
+    const float mn = fmaxf(fmaxf(m, fmaxf(li[0], li[1])), fmaxf(li[2], li[3]));
+    if (mn == neg_inf()) continue;
+    const float shrink = m == neg_inf() ? 0.f : ex2((m - mn) * kLog2e);
+    sum *= shrink;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] *= shrink;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float wt = li[u] == neg_inf() ? 0.f : ex2((li[u] - mn) * kLog2e);
+      sum += wt;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[4 * k + 0] = fmaf(wt, x[u][k].x, acc[4 * k + 0]);
+        acc[4 * k + 1] = fmaf(wt, x[u][k].y, acc[4 * k + 1]);
+        acc[4 * k + 2] = fmaf(wt, x[u][k].z, acc[4 * k + 2]);
+        acc[4 * k + 3] = fmaf(wt, x[u][k].w, acc[4 * k + 3]);
+      }
+    }
+    m = mn;
   }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] *= inv;
+  const float LSE = sum > 0.f ? m + lg2(sum) * kLn2 : neg_inf();
   const int64_t orow = ((int64_t)q0 + tok) * a.Hq + (int64_t)job.h * a.G + r % a.G;
   uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kHeadDim + d0);
   dst[0] = make_uint4(cvt_bf16x2(acc[0], acc[1]), cvt_bf16x2(acc[2], acc[3]),

@@ -427,6 +427,9 @@ __global__ void varlen_fixup_kernel(const int* __restrict__ desc, const float* _
                                     const int32_t* __restrict__ cu_seqlens_q, int num_workers,
                                     int Hq, int G, int QT, uint16_t* __restrict__ out,
                                     float* __restrict__ lse) {
+  // the next grid in the stream may start its own preparation now; it waits
+  // for this grid before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
