@@ -63,6 +63,18 @@ def decode_algorithmic_bytes(w) -> int:
     return kv + q_out + tables
 
 
+def decode_algorithmic_bytes_int8(w) -> int:
+    """As decode_algorithmic_bytes for the int8 pool: 1-byte K and V codes plus
+    one fp32 scale per (token, KV head) row each (2112 B per token)."""
+    ctx = w.context_lens.to(torch.int64)
+    kv = int(ctx.sum()) * w.num_kv_heads * (w.head_dim + 4) * 2
+    S, Hq, D = w.num_seqs, w.num_q_heads, w.head_dim
+    rows = w.num_q_tokens
+    q_out = rows * Hq * D * 2 * 2 + rows * Hq * 4
+    tables = int(((ctx + w.block_size - 1) // w.block_size).sum()) * 4 + S * 4
+    return kv + q_out + tables
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -396,6 +408,65 @@ def run_secondary(args, dev, B):
         del kc, vc
         torch.cuda.empty_cache()
     res.update(run_secondary_varlen(args, dev, B, peak))
+    res.update(run_secondary_int8(args, dev, B, peak))
+    return res
+
+
+def run_secondary_int8(args, dev, B, peak):
+    """Decode over the INT8 pool (quantised cache write, fused dequant): the
+    engine batch rotated over 4 layer pools, the ragged and the long batch."""
+    from paged_kv_decode_18_gb300 import workloads as W
+
+    res = {}
+    for name, make, nlayers in (("engine", W.engine, LAYERS), ("ragged", W.ragged, 1),
+                                ("long", W.long, 1)):
+        w = make(seed=args.seed)
+        pools = []
+        for _ in range(nlayers):
+            kc, vc, ks, vs = w.empty_pool_i8(dev)
+            B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
+                                        kc, vc, ks, vs)
+            B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev),
+                                        kc, vc, ks, vs)
+            pools.append((kc, vc, ks, vs))
+        q = w.q.to(dev)
+        bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        sh = B.shape_of(q, pools[0][0], bt)
+        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
+
+        def call(l):
+            kc, vc, ks, vs = pools[l]
+            B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse, num_splits=0,
+                             workspace=ws)
+        per_replay = 4 if nlayers > 1 else 2
+        call(0)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(per_replay):
+                call(i % nlayers)
+        for _ in range(5):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(30)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1_000_000)
+        for a, b in evs:
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / per_replay
+        alg = decode_algorithmic_bytes_int8(w)
+        gbs = alg / (ms / 1e3) / 1e9
+        res[f"{name}_int8"] = {"decode_ms": round(ms, 5), "alg_bytes": alg,
+                               "achieved_gbs": round(gbs, 1),
+                               "frac_of_measured_peak": round(gbs / peak, 4),
+                               "tokens_per_s": w.num_q_tokens / (ms / 1e3),
+                               "kv_format": "int8 + fp32 row scales"}
+        del pools
+        torch.cuda.empty_cache()
     return res
 
 

@@ -43,7 +43,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", "-Wall",
            "-Wextra", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
@@ -69,6 +69,14 @@ def _load():
             P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, dbl, i32, i32, i64, i32, P, P]
         lib.pa_oracle_splitk_merge.restype = i32
         lib.pa_oracle_splitk_merge.argtypes = [P, P, i64, i32, i32, P, P]
+        lib.pa_oracle_quantize_rows_i8.restype = i32
+        lib.pa_oracle_quantize_rows_i8.argtypes = [P, i64, i32, P, P]
+        lib.pa_oracle_reshape_and_cache_i8.restype = i32
+        lib.pa_oracle_reshape_and_cache_i8.argtypes = [P, P, P, i64, i32, i32, i32, i64, P, P,
+                                                       P, P]
+        lib.pa_oracle_paged_attention_i8.restype = i32
+        lib.pa_oracle_paged_attention_i8.argtypes = [
+            P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, dbl, i32, i32, P, P]
         _lib = lib
         return lib
 
@@ -185,4 +193,66 @@ def splitk_merge(part_out: np.ndarray, part_lse: np.ndarray):
     lse = np.zeros(rows, np.float64)
     _check(lib.pa_oracle_splitk_merge(_ptr(po), _ptr(pl), rows, P, D, _ptr(out), _ptr(lse)),
            "splitk_merge")
+    return out, lse
+
+
+def quantize_rows_i8(x):
+    """Quantise rows of bf16 values (last axis = one group) -> (codes int8, scales fp32).
+
+    Rule (see pa_oracle.c): amax = max |x|; inv = fl32(127 / amax);
+    code = clamp(rint(fl32(x * inv)), -127, 127); scale = fl32(amax / 127).
+    """
+    lib = _load()
+    x16 = _as_u16(x)
+    D = x16.shape[-1]
+    rows = x16.size // D
+    codes = np.zeros(x16.shape, np.int8)
+    scales = np.zeros(x16.shape[:-1], np.float32)
+    _check(lib.pa_oracle_quantize_rows_i8(_ptr(x16), rows, D, _ptr(codes), _ptr(scales)),
+           "quantize_rows_i8")
+    return codes, scales
+
+
+def reshape_and_cache_i8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale) -> None:
+    """Quantising cache write into int8 pools (numpy arrays, updated in place)."""
+    lib = _load()
+    k16, v16 = _as_u16(k), _as_u16(v)
+    sm = _as(slot_mapping, np.int64)
+    for a, dt in ((k_cache, np.int8), (v_cache, np.int8), (k_scale, np.float32),
+                  (v_scale, np.float32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise ValueError("int8 pool arrays must be contiguous int8 / float32")
+    T, Hkv, D = k16.shape
+    NB, Hkv2, BS, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or k_scale.shape != (NB, Hkv, BS):
+        raise ValueError("cache shape mismatch")
+    _check(lib.pa_oracle_reshape_and_cache_i8(_ptr(k16), _ptr(v16), _ptr(sm), T, Hkv, D, BS, NB,
+                                              _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                              _ptr(v_scale)), "reshape_and_cache_i8")
+
+
+def paged_attention_i8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                       cu_seqlens_q, scale: float, causal: bool = True, num_threads: int = 0):
+    """Paged attention in fp64 over int8 pools (rows dequantised as code * scale)."""
+    lib = _load()
+    q16 = _as_u16(q)
+    kc, vc = _as(k_cache, np.int8), _as(v_cache, np.int8)
+    ks, vs = _as(k_scale, np.float32), _as(v_scale, np.float32)
+    bt = _as(block_tables, np.int32)
+    cl = _as(context_lens, np.int32)
+    cu = _as(cu_seqlens_q, np.int32)
+    Tq, Hq, D = q16.shape
+    NB, Hkv, BS, D2 = kc.shape
+    if D2 != D or vc.shape != kc.shape or ks.shape != (NB, Hkv, BS) or vs.shape != ks.shape:
+        raise ValueError("cache shape mismatch")
+    S = cl.shape[0]
+    if bt.ndim != 2 or bt.shape[0] != S or cu.shape[0] != S + 1 or int(cu[-1]) != Tq:
+        raise ValueError("table / length shape mismatch")
+    out = np.zeros((Tq, Hq, D), np.float64)
+    lse = np.zeros((Tq, Hq), np.float64)
+    rc = lib.pa_oracle_paged_attention_i8(
+        _ptr(q16), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(cl), _ptr(cu), S, Hq,
+        Hkv, D, BS, bt.shape[1], NB, float(scale), 1 if causal else 0, int(num_threads),
+        _ptr(out), _ptr(lse))
+    _check(rc, "paged_attention_i8")
     return out, lse

@@ -38,6 +38,17 @@
  *   tiles with a running max and running sum. It exists only so the tests can
  *   check it against the two-pass routine.
  *
+ *   INT8 KV rows (course README, curriculum row "Memory & KV Cache":
+ *   quantization; the "INT8 KV" configuration; claim "s08": grouping keeps
+ *   outliers in check). The pages fix no formula; the reading used here is
+ *   the plainest one: symmetric quantisation with one group per (token, KV
+ *   head) row of head_dim values, every step one IEEE fp32 operation:
+ *     amax = max_d |x_d|;  amax == 0 -> all codes 0 and scale 0; else
+ *     inv = 127 / amax,  code_d = clamp(rint(x_d * inv), -127, 127),
+ *     scale = amax / 127   (rint: nearest, ties to even).
+ *   A row dequantises to code_d * scale (exact in fp64). Attention over an
+ *   int8 pool is the attention above over the dequantised rows.
+ *
  * Numbers: bf16 inputs are bit patterns (uint16). They are widened to fp64
  * exactly (bf16 -> fp32 is a 16-bit shift; fp32 -> fp64 is exact).
  */
@@ -60,6 +71,13 @@ static double bf16_bits_to_double(uint16_t bits) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+static float bf16_bits_to_float(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
 }
 
 int pa_oracle_max_threads(void) {
@@ -97,6 +115,65 @@ int pa_oracle_reshape_and_cache(const uint16_t *k, const uint16_t *v,
                 k_cache[dst] = k[src];
                 v_cache[dst] = v[src];
             }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* INT8 quantisation of one row of D bf16 values (rule in the header).       */
+/* ------------------------------------------------------------------------ */
+static void quantize_row_i8(const uint16_t *x, int D, int8_t *codes, float *scale) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(bf16_bits_to_float(x[d]));
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        for (int d = 0; d < D; ++d) codes[d] = 0;
+        *scale = 0.0f;
+        return;
+    }
+    float inv = 127.0f / amax;
+    for (int d = 0; d < D; ++d) {
+        float t = rintf(bf16_bits_to_float(x[d]) * inv);
+        if (t > 127.0f) t = 127.0f;
+        if (t < -127.0f) t = -127.0f;
+        codes[d] = (int8_t)t;
+    }
+    *scale = amax / 127.0f;
+}
+
+/* rows [rows][D] bf16 -> codes [rows][D] int8, scales [rows] fp32 */
+int pa_oracle_quantize_rows_i8(const uint16_t *x, int64_t rows, int D, int8_t *codes,
+                               float *scales) {
+    if (rows < 0 || D <= 0) return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        quantize_row_i8(x + r * D, D, codes + r * D, scales + r);
+    return ORACLE_OK;
+}
+
+/* Cache write into the int8 pool: row k[t][h][:] is quantised into         */
+/* k_cache[slot / BS][h][slot % BS][:] and k_scale[slot / BS][h][slot % BS]. */
+int pa_oracle_reshape_and_cache_i8(const uint16_t *k, const uint16_t *v,
+                                   const int64_t *slot_mapping, int64_t num_tokens,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int64_t num_blocks, int8_t *k_cache, int8_t *v_cache,
+                                   float *k_scale, float *v_scale) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * (int64_t)block_size) return ORACLE_ERR_RANGE;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t src = (t * num_kv_heads + h) * (int64_t)head_dim;
+            int64_t row = (block * num_kv_heads + h) * (int64_t)block_size + offset;
+            quantize_row_i8(k + src, head_dim, k_cache + row * head_dim, k_scale + row);
+            quantize_row_i8(v + src, head_dim, v_cache + row * head_dim, v_scale + row);
         }
     }
     return ORACLE_OK;
@@ -212,13 +289,15 @@ int pa_oracle_attention_dense(const uint16_t *q, const uint16_t *K, const uint16
 /* Query head h reads KV head h / (Hq / Hkv).                                */
 /* mode 0 = two-pass (the oracle proper); mode 1 = online with `tile` keys.  */
 /* ------------------------------------------------------------------------ */
-int pa_oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
-                              const uint16_t *v_cache, const int32_t *block_tables,
-                              const int32_t *context_lens, const int32_t *cu_seqlens_q,
-                              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int block_size, int max_blocks_per_seq, int64_t num_blocks,
-                              double scale, int causal, int mode, int64_t tile,
-                              int num_threads, double *out, double *lse) {
+/* Pool element formats: bf16 (k16/v16) or int8 rows with one scale per row. */
+static int paged_attention_core(const uint16_t *q, const uint16_t *k16, const uint16_t *v16,
+                                const int8_t *k8, const int8_t *v8, const float *k_scale,
+                                const float *v_scale, const int32_t *block_tables,
+                                const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                double scale, int causal, int mode, int64_t tile,
+                                int num_threads, double *out, double *lse) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || max_blocks_per_seq < 0 || num_q_heads % num_kv_heads != 0 ||
         (mode == 1 && tile <= 0))
@@ -265,10 +344,16 @@ int pa_oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
         /* gather this sequence's context for KV head kvh, in position order */
         for (int64_t p = 0; p < c; ++p) {
             int64_t phys = block_tables[(int64_t)s * max_blocks_per_seq + p / block_size];
-            int64_t row = ((phys * num_kv_heads + kvh) * block_size + p % block_size) * D;
+            int64_t srow = (phys * num_kv_heads + kvh) * block_size + p % block_size;
+            int64_t row = srow * D;
             for (int d = 0; d < D; ++d) {
-                K[p * D + d] = bf16_bits_to_double(k_cache[row + d]);
-                V[p * D + d] = bf16_bits_to_double(v_cache[row + d]);
+                if (k16) {
+                    K[p * D + d] = bf16_bits_to_double(k16[row + d]);
+                    V[p * D + d] = bf16_bits_to_double(v16[row + d]);
+                } else {  /* dequantised int8 row: code * scale, exact in fp64 */
+                    K[p * D + d] = (double)k8[row + d] * (double)k_scale[srow];
+                    V[p * D + d] = (double)v8[row + d] * (double)v_scale[srow];
+                }
             }
         }
         for (int g = 0; g < G; ++g) {
@@ -290,6 +375,36 @@ int pa_oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
         free(K); free(V); free(qd); free(tmp);
     }
     return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+int pa_oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *block_tables,
+                              const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                              double scale, int causal, int mode, int64_t tile,
+                              int num_threads, double *out, double *lse) {
+    return paged_attention_core(q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_tables,
+                                context_lens, cu_seqlens_q, num_seqs, num_q_heads,
+                                num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                num_blocks, scale, causal, mode, tile, num_threads, out, lse);
+}
+
+/* Paged attention over an int8 pool (rows dequantised as code * scale). */
+int pa_oracle_paged_attention_i8(const uint16_t *q, const int8_t *k_cache,
+                                 const int8_t *v_cache, const float *k_scale,
+                                 const float *v_scale, const int32_t *block_tables,
+                                 const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                 double scale, int causal, int num_threads, double *out,
+                                 double *lse) {
+    if (!k_cache || !v_cache || !k_scale || !v_scale) return ORACLE_ERR_ARG;
+    return paged_attention_core(q, NULL, NULL, k_cache, v_cache, k_scale, v_scale,
+                                block_tables, context_lens, cu_seqlens_q, num_seqs,
+                                num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, scale, causal, 0, 0,
+                                num_threads, out, lse);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -41,6 +41,9 @@ EXPORTED = (
     "pa_append_decode",
     "pa_decode_varlen",
     "pa_decode_varlen_workspace_size",
+    "pa_reshape_and_cache_int8",
+    "pa_decode_int8",
+    "pa_decode_int8_workspace_size",
     "pa_splitk_reduce",
     "pa_status_string",
     "pa_debug_read_error",
@@ -98,6 +101,12 @@ def load(path: str | None = None):
         lib.pa_decode_varlen.argtypes = [V, V, V, V, V, V, i64, i32, i32, f32, V, V, S, V, sz, V]
         lib.pa_decode_varlen_workspace_size.restype = sz
         lib.pa_decode_varlen_workspace_size.argtypes = [S, i64, i32]
+        lib.pa_reshape_and_cache_int8.restype = i32
+        lib.pa_reshape_and_cache_int8.argtypes = [V, V, V, i64, V, V, V, V, S, V]
+        lib.pa_decode_int8.restype = i32
+        lib.pa_decode_int8.argtypes = [V, V, V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
+        lib.pa_decode_int8_workspace_size.restype = sz
+        lib.pa_decode_int8_workspace_size.argtypes = [S, i32]
         lib.pa_splitk_reduce.restype = i32
         lib.pa_splitk_reduce.argtypes = [V, V, i64, i32, i32, i32, V, V, V]
         lib.pa_status_string.restype = ctypes.c_char_p
@@ -197,6 +206,63 @@ def pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None) -> N
 
 def pa_decode_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
     return int(load().pa_decode_workspace_size(ctypes.byref(shape), int(num_splits)))
+
+
+def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                              stream=None) -> None:
+    """Quantising cache write into the int8 pool (one fp32 scale per row)."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_cache, "k_cache", torch.int8, 4)
+    _need(v_cache, "v_cache", torch.int8, 4)
+    _need(k_scale, "k_scale", torch.float32, 3)
+    _need(v_scale, "v_scale", torch.float32, 3)
+    if k.shape != v.shape or k_cache.shape != v_cache.shape or k_scale.shape != v_scale.shape:
+        raise ValueError("k/v, cache or scale shapes differ")
+    if slot_mapping.shape[0] != k.shape[0]:
+        raise ValueError("slot_mapping length != number of tokens")
+    NB, Hkv, BS, D = k_cache.shape
+    if k.shape[1:] != (Hkv, D) or k_scale.shape != (NB, Hkv, BS):
+        raise ValueError("k rows or scales do not match the cache")
+    sh = make_shape(0, Hkv, Hkv, D, BS, 0, NB)
+    _check(load().pa_reshape_and_cache_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
+                                            _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                            _ptr(v_scale), ctypes.byref(sh), _stream(stream)),
+           "pa_reshape_and_cache_int8")
+
+
+def pa_decode_int8_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
+    return int(load().pa_decode_int8_workspace_size(ctypes.byref(shape), int(num_splits)))
+
+
+def pa_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                   out, lse=None, num_splits: int = 0, workspace=None, stream=None) -> None:
+    """Decode over the int8 pool with the dequantisation fused."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.int8, 4)
+    _need(v_cache, "v_cache", torch.int8, 4)
+    _need(k_scale, "k_scale", torch.float32, 3)
+    _need(v_scale, "v_scale", torch.float32, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    if k_cache.shape != v_cache.shape or k_scale.shape != k_cache.shape[:3] or \
+            v_scale.shape != k_scale.shape:
+        raise ValueError("cache / scale shapes differ")
+    sh = shape_of(q, k_cache, block_tables)
+    if q.shape[0] != sh.num_seqs or context_lens.shape[0] != sh.num_seqs:
+        raise ValueError("q / context_lens rows != number of sequences")
+    if out.shape != q.shape:
+        raise ValueError("out shape != q shape")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_int8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                 _ptr(v_scale), _ptr(block_tables), _ptr(context_lens),
+                                 float(scale), _ptr(out), _ptr(lse), ctypes.byref(sh),
+                                 int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)),
+           "pa_decode_int8")
 
 
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,

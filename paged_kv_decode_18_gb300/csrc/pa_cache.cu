@@ -43,6 +43,62 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
   v_cache[dst] = v[i];
 }
 
+// Quantising write (INT8 KV): one warp per (token, KV head) row of 128 values.
+// Symmetric, one fp32 scale per row: amax = max |x|, q = rint(x * (127 / amax))
+// clamped to [-127, 127], scale = amax / 127; a zero row stores q = 0 and
+// scale = 0. Division and product are IEEE-rounded fp32 operations (explicit
+// _rn intrinsics, no contraction), rint rounds half to even. The row lands
+// as 128 contiguous bytes of the (block, KV head) int8 tile and one float of
+// the [num_blocks][Hkv][16] scale array.
+__device__ __forceinline__ void quantize_row_to(const uint2 x, int lane, int8_t* __restrict__ dst,
+                                                float* __restrict__ scale_dst) {
+  const float f0 = bf_lo(x.x), f1 = bf_hi(x.x), f2 = bf_lo(x.y), f3 = bf_hi(x.y);
+  float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+  uint32_t packed = 0u;
+  if (amax > 0.f) {
+    const float inv = __fdiv_rn(127.f, amax);
+    const float fs[4] = {f0, f1, f2, f3};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float t = fminf(fmaxf(rintf(__fmul_rn(fs[j], inv)), -127.f), 127.f);
+      packed |= ((uint32_t)(int)t & 0xffu) << (8 * j);
+    }
+  }
+  reinterpret_cast<uint32_t*>(dst)[lane] = packed;
+  if (lane == 0) *scale_dst = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
+}
+
+__global__ void reshape_and_cache_int8_kernel(const uint2* __restrict__ k,
+                                              const uint2* __restrict__ v,
+                                              const int64_t* __restrict__ slots, int64_t rows,
+                                              int Hkv, int64_t num_slots,
+                                              int8_t* __restrict__ k_cache,
+                                              int8_t* __restrict__ v_cache,
+                                              float* __restrict__ k_scale,
+                                              float* __restrict__ v_scale) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;  // warp-uniform
+  const int64_t t = row / Hkv;
+  const int h = (int)(row - t * Hkv);
+  const int64_t slot = slots[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) flag_error(PA_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const int64_t blk = slot / kBlock, off = slot % kBlock;
+  const int64_t dst_row = (blk * Hkv + h) * kBlock + off;  // row index in [NB][Hkv][16]
+  // lane reads dims 4*lane .. 4*lane+3 (8 bytes): the warp reads the 256-byte row
+  const uint2 xk = k[row * 32 + lane], xv = v[row * 32 + lane];
+  quantize_row_to(xk, lane, k_cache + dst_row * kHeadDim, k_scale + dst_row);
+  quantize_row_to(xv, lane, v_cache + dst_row * kHeadDim, v_scale + dst_row);
+}
+
 }  // namespace
 
 unsigned take_error_word_cache(cudaStream_t stream, int* rc) {
@@ -82,6 +138,32 @@ extern "C" int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v,
                        shape->num_kv_heads, shape->num_blocks * shape->block_size,
                        reinterpret_cast<uint4*>(k_cache),
                        reinterpret_cast<uint4*>(v_cache)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v,
+                                         const int64_t* slot_mapping, int64_t num_tokens,
+                                         int8_t* k_cache, int8_t* v_cache, float* k_scale,
+                                         float* v_scale, const pa_shape* shape, void* stream) {
+  int rc = check_shape_common(shape);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PA_ERR_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(k_scale, 16) || !aligned(v_scale, 16) || !aligned(slot_mapping, 8))
+    return PA_ERR_ARG;
+  const int64_t rows = num_tokens * shape->num_kv_heads;
+  const int wpb = 8;
+  const int64_t blocks = (rows + wpb - 1) / wpb;
+  if (blocks > 0x7fffffff) return PA_ERR_ARG;
+  if (launch_dependent(reshape_and_cache_int8_kernel, dim3((unsigned)blocks), dim3(wpb * 32), 0,
+                       static_cast<cudaStream_t>(stream), reinterpret_cast<const uint2*>(k),
+                       reinterpret_cast<const uint2*>(v), slot_mapping, rows,
+                       shape->num_kv_heads, shape->num_blocks * shape->block_size, k_cache,
+                       v_cache, k_scale, v_scale) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -36,10 +36,21 @@ namespace {
 
 constexpr int kG = 2;                          // query heads per KV head (built)
 constexpr int kQBytes = kG * kHeadDim * 2;     // 512
-constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
 
-template <int NSTAGE>
+// Stage layout for a KV element format: bf16 tiles (4 KB each), or int8
+// tiles (2 KB each) followed by the tile's 16 K scales and 16 V scales.
+template <bool Q8>
+struct KvFormat {
+  static constexpr int kTile = Q8 ? kBlock * kHeadDim : kTileBytes;  // one K or V tile, bytes
+  static constexpr int kRow = kTile / kBlock;                        // one token row, bytes
+  static constexpr int kScaleOff = 2 * kTile;
+  static constexpr int kQOff = kScaleOff + (Q8 ? 2 * kBlock * 4 : 0);
+  static constexpr int kStage = kQOff + kQBytes;
+};
+
+template <int NSTAGE, bool Q8>
 struct WarpLayout {
+  static constexpr int kStageBytes = KvFormat<Q8>::kStage;
   static constexpr int kBarOff = NSTAGE * kStageBytes;
   static constexpr int kPOff = kBarOff + ((NSTAGE * 8 + 15) / 16) * 16;
   static constexpr int kBytes = ((kPOff + 128 + 127) / 128) * 128;
@@ -49,8 +60,10 @@ enum : int { kBalanced = 0, kFixed = 1 };
 
 struct DecodeArgs {
   const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  const unsigned char* k_cache;  // bf16 or int8 tiles
+  const unsigned char* v_cache;
+  const float* k_scale;          // int8: [num_blocks][Hkv][16] per-row scales
+  const float* v_scale;
   const int32_t* block_tables;
   const int32_t* context_lens;
   uint16_t* out;
@@ -81,9 +94,42 @@ __device__ __forceinline__ void store_f8(float* dst, const float (&v)[8], float 
   reinterpret_cast<float4*>(dst)[1] = make_float4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
 }
 
-template <int NWARPS, int NSTAGE>
+// Four signed bytes -> two float pairs, exactly: the byte (biased by 128)
+// becomes the low mantissa bits of 2^23, one packed subtraction removes both.
+__device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& lo, float2& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const float2 bias = make_float2(-8388736.f, -8388736.f);  // 2^23 + 128
+  lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                              __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
+                  bias);
+  hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                              __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
+                  bias);
+}
+
+// The 16 dims 16*c8 .. 16*c8+15 of one token row in stage memory, as 8 pairs.
+template <bool Q8>
+__device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)[8]) {
+  if constexpr (Q8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row);
+    i8x4_to_f2(w.x, f[0], f[1]);
+    i8x4_to_f2(w.y, f[2], f[3]);
+    i8x4_to_f2(w.z, f[4], f[5]);
+    i8x4_to_f2(w.w, f[6], f[7]);
+  } else {
+    const uint4 wa = *reinterpret_cast<const uint4*>(row);
+    const uint4 wb = *reinterpret_cast<const uint4*>(row + 16);
+    const uint32_t wk[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = make_float2(bf_lo(wk[j]), bf_hi(wk[j]));
+  }
+}
+
+template <int NWARPS, int NSTAGE, bool Q8>
 __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeArgs a) {
-  using L = WarpLayout<NSTAGE>;
+  using L = WarpLayout<NSTAGE, Q8>;
+  using F = KvFormat<Q8>;
+  constexpr int kStageBytes = F::kStage;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* wbuf = smem + warp * L::kBytes;
@@ -208,12 +254,17 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
       unsigned char* st = wbuf + stage * kStageBytes;
       const uint32_t bar = smem_addr(&bars[stage]);
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, 2 * kTileBytes + (first ? kQBytes : 0));
-      const size_t tile = ((size_t)phys * Hkv + pp.h) * (kBlock * kHeadDim);
-      bulk_copy_g2s(smem_addr(st), a.k_cache + tile, kTileBytes, bar);
-      bulk_copy_g2s(smem_addr(st + kTileBytes), a.v_cache + tile, kTileBytes, bar);
+      mbar_arrive_expect_tx(bar, F::kQOff + (first ? kQBytes : 0));
+      const size_t tile = (size_t)phys * Hkv + pp.h;
+      bulk_copy_g2s(smem_addr(st), a.k_cache + tile * F::kTile, F::kTile, bar);
+      bulk_copy_g2s(smem_addr(st + F::kTile), a.v_cache + tile * F::kTile, F::kTile, bar);
+      if constexpr (Q8) {
+        bulk_copy_g2s(smem_addr(st + F::kScaleOff), a.k_scale + tile * kBlock, kBlock * 4, bar);
+        bulk_copy_g2s(smem_addr(st + F::kScaleOff + kBlock * 4), a.v_scale + tile * kBlock,
+                      kBlock * 4, bar);
+      }
       if (first)
-        bulk_copy_g2s(smem_addr(st + 2 * kTileBytes),
+        bulk_copy_g2s(smem_addr(st + F::kQOff),
                       a.q + ((size_t)pp.s * Hq + (size_t)pp.h * kG) * kHeadDim, kQBytes, bar);
     }
     ++pidx;
@@ -253,7 +304,7 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     if (first) {
 #pragma unroll
       for (int g = 0; g < kG; ++g) {
-        const uint4* qs = reinterpret_cast<const uint4*>(st + 2 * kTileBytes + g * 256 + c8 * 32);
+        const uint4* qs = reinterpret_cast<const uint4*>(st + F::kQOff + g * 256 + c8 * 32);
         const uint4 qa = qs[0], qb = qs[1];
         const uint32_t wq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
@@ -272,18 +323,16 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
 
     // ---- scores: 4 tokens x 2 heads of partial dots per lane ----------------
     float sc[8];
-    const unsigned char* Ks = st + grp * 4 * 256 + c8 * 32;
+    const unsigned char* Ks = st + grp * 4 * F::kRow + c8 * (F::kRow / 8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 ka = *reinterpret_cast<const uint4*>(Ks + i * 256);
-      const uint4 kb = *reinterpret_cast<const uint4*>(Ks + i * 256 + 16);
-      const uint32_t wk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+      float2 kf[8];
+      load_row16<Q8>(Ks + i * F::kRow, kf);
       float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float2 kf = make_float2(bf_lo(wk[j]), bf_hi(wk[j]));
-        d0 = __ffma2_rn(q2[0][j], kf, d0);
-        d1 = __ffma2_rn(q2[1][j], kf, d1);
+        d0 = __ffma2_rn(q2[0][j], kf[j], d0);
+        d1 = __ffma2_rn(q2[1][j], kf[j], d1);
       }
       sc[2 * i] = d0.x + d0.y;
       sc[2 * i + 1] = d1.x + d1.y;
@@ -302,7 +351,10 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
       }
     }
     const int tok = grp * 4 + ((lane & 7) >> 1);
-    const float s_val = tok < nvalid ? sc[0] : neg_inf();
+    // int8: the row's K scale multiplies its dot product
+    float s_val = sc[0];
+    if constexpr (Q8) s_val *= reinterpret_cast<const float*>(st + F::kScaleOff)[tok];
+    s_val = tok < nvalid ? s_val : neg_inf();
 
     // ---- online softmax (log2 domain) ------------------------------------------
     float mx = s_val;
@@ -335,21 +387,23 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
       }
     }
     // ---- PV ----------------------------------------------------------------------
-    const unsigned char* Vs = st + kTileBytes + grp * 4 * 256 + c8 * 32;
+    const unsigned char* Vs = st + F::kTile + grp * 4 * F::kRow + c8 * (F::kRow / 8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // tokens past the context may hold anything (even NaN): skip, never 0*x
       if (nvalid == kBlock || grp * 4 + i < nvalid) {
-        const uint4 va = *reinterpret_cast<const uint4*>(Vs + i * 256);
-        const uint4 vb = *reinterpret_cast<const uint4*>(Vs + i * 256 + 16);
-        const uint32_t wv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-        const float2 p0 = make_float2(pv[2 * i], pv[2 * i]);
-        const float2 p1 = make_float2(pv[2 * i + 1], pv[2 * i + 1]);
+        float2 vf[8];
+        load_row16<Q8>(Vs + i * F::kRow, vf);
+        // int8: the row's V scale folds into its weights
+        float vsc = 1.f;
+        if constexpr (Q8)
+          vsc = reinterpret_cast<const float*>(st + F::kScaleOff + kBlock * 4)[grp * 4 + i];
+        const float2 p0 = make_float2(pv[2 * i] * vsc, pv[2 * i] * vsc);
+        const float2 p1 = make_float2(pv[2 * i + 1] * vsc, pv[2 * i + 1] * vsc);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float2 vf = make_float2(bf_lo(wv[j]), bf_hi(wv[j]));
-          acc[0][j] = __ffma2_rn(p0, vf, acc[0][j]);
-          acc[1][j] = __ffma2_rn(p1, vf, acc[1][j]);
+          acc[0][j] = __ffma2_rn(p0, vf[j], acc[0][j]);
+          acc[1][j] = __ffma2_rn(p1, vf[j], acc[1][j]);
         }
       }
     }
@@ -358,7 +412,7 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
     if (last) {
       // ---- finish the piece: combine the 4 token groups through this stage's
-      // (already consumed) K buffer, then each lane owns 8 outputs ------------
+      // (already consumed) K/V buffers, 4 KB, then each lane owns 8 outputs ----
       float* red = reinterpret_cast<float*>(st);  // [grp][g][128] fp32 = 4 KB
 #pragma unroll
       for (int g = 0; g < kG; ++g) {
@@ -572,7 +626,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part_o,
 // host side
 // ---------------------------------------------------------------------------
 constexpr int kWarps = 6;
-constexpr int kStages = 2;
+constexpr int kStages = 2;    // bf16: 2 x 8 KB of copies in flight per warp
+constexpr int kStagesQ8 = 3;  // int8: 3 x 4 KB (two CTAs per SM still fit)
 
 struct DecodeGeometry {
   int mode = kBalanced;
@@ -586,13 +641,15 @@ struct DecodeGeometry {
 
 inline size_t plan_smem_bytes(int S) { return sizeof(int) * (4 * (size_t)S + 3 + 40); }
 
-int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
+template <bool Q8>
+int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
+  constexpr int NST = Q8 ? kStagesQ8 : kStages;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
-  g->smem = (size_t)kWarps * WarpLayout<kStages>::kBytes + plan_smem_bytes(S);
+  g->smem = (size_t)kWarps * WarpLayout<NST, Q8>::kBytes + plan_smem_bytes(S);
   if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
-  auto kern = paged_decode_kernel<kWarps, kStages>;
+  auto kern = paged_decode_kernel<kWarps, NST, Q8>;
   static std::mutex mu;
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -636,6 +693,10 @@ int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
   return PA_OK;
 }
 
+int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool q8 = false) {
+  return q8 ? decode_geometry_t<true>(sh, num_splits, g) : decode_geometry_t<false>(sh, num_splits, g);
+}
+
 int check_decode_args(const pa_shape* shape, int num_splits) {
   int rc = check_shape_common(shape);
   if (rc != PA_OK) return rc;
@@ -672,25 +733,38 @@ extern "C" size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits
   return g.ws_bytes;
 }
 
+extern "C" size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_splits) {
+  if (check_decode_args(shape, num_splits) != PA_OK) return 0;
+  if (shape->num_seqs == 0) return 0;
+  DecodeGeometry g;
+  if (decode_geometry(shape, num_splits, &g, true) != PA_OK) return 0;
+  return g.ws_bytes;
+}
+
 namespace pa {
 namespace {
 
 // Validate, size and launch the decode grid and its merge. `early`: see the
 // kernel (only pa_append_decode sets it).
-int decode_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
-                const int32_t* block_tables, const int32_t* context_lens, float scale,
-                pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
-                void* workspace, size_t workspace_bytes, cudaStream_t st, int early) {
+// k_scale / v_scale non-null selects the int8 format.
+int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
+                const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                const int32_t* context_lens, float scale, pa_bf16* out, float* lse,
+                const pa_shape* shape, int num_splits, void* workspace, size_t workspace_bytes,
+                cudaStream_t st, int early) {
+  const bool q8 = k_scale != nullptr;
   int rc = check_decode_args(shape, num_splits);
   if (rc != PA_OK) return rc;
   if (shape->num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
+  if (q8 && !v_scale) return PA_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (lse && !aligned(lse, 4)))
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (lse && !aligned(lse, 4)) ||
+      (q8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))))
     return PA_ERR_ARG;
   if (!(scale == scale)) return PA_ERR_ARG;
   DecodeGeometry g;
-  rc = decode_geometry(shape, num_splits, &g);
+  rc = decode_geometry(shape, num_splits, &g, q8);
   if (rc != PA_OK) return rc;
   if (g.ws_bytes > 0 &&
       (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256)))
@@ -698,8 +772,10 @@ int decode_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
 
   DecodeArgs a;
   a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
+  a.k_cache = static_cast<const unsigned char*>(k_cache);
+  a.v_cache = static_cast<const unsigned char*>(v_cache);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = out;
@@ -718,9 +794,12 @@ int decode_impl(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
   a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
   a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
 
-  if (launch_dependent(paged_decode_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
-                       g.smem, st, a) != cudaSuccess)
-    return PA_ERR_CUDA;
+  const cudaError_t le =
+      q8 ? launch_dependent(paged_decode_kernel<kWarps, kStagesQ8, true>, dim3(g.grid),
+                            dim3(kWarps * 32), g.smem, st, a)
+         : launch_dependent(paged_decode_kernel<kWarps, kStages, false>, dim3(g.grid),
+                            dim3(kWarps * 32), g.smem, st, a);
+  if (le != cudaSuccess) return PA_ERR_CUDA;
   const int wpb = 8;
   if (g.mode == kBalanced) {
     // the merge grid may be scheduled while the decode grid drains; it waits
@@ -746,9 +825,21 @@ extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
                          const int32_t* block_tables, const int32_t* context_lens, float scale,
                          pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape,
-                     num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
-                     0);
+  return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
+                     out, lse, shape, num_splits, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), 0);
+}
+
+extern "C" int pa_decode_int8(const pa_bf16* q, const int8_t* k_cache, const int8_t* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!k_scale || !v_scale) return PA_ERR_ARG;
+  return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                     out, lse, shape, num_splits, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), 0);
 }
 
 extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
@@ -778,9 +869,9 @@ extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
   if (rc != PA_OK) return rc;
   // with new tokens, the cache write ran just before: the decode prologue
   // (which reads only context_lens and block_tables) may overlap it
-  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape, 0,
-                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
-                     num_new_tokens > 0 ? 1 : 0);
+  return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
+                     out, lse, shape, 0, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), num_new_tokens > 0 ? 1 : 0);
 }
 
 extern "C" int pa_splitk_reduce(const float* part_out, const float* part_lse, int64_t num_rows,

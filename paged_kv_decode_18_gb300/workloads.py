@@ -34,6 +34,7 @@ from dataclasses import dataclass, field
 import torch
 
 POOL_SENTINEL_BITS = 0x7FC0  # bf16 quiet NaN
+POOL_SENTINEL_CODE = -128    # int8 pools
 
 NUM_Q_HEADS = 16
 NUM_KV_HEADS = 8
@@ -88,6 +89,15 @@ class Workload:
                           device=device)
         pool = pool.view(torch.bfloat16)
         return pool, pool.clone()
+
+    def empty_pool_i8(self, device="cpu"):
+        """An int8 pool (k codes, v codes, k scales, v scales). Unwritten codes
+        hold -128 (never produced by the quantiser) and unwritten scales NaN."""
+        codes = torch.full(self.pool_shape(), POOL_SENTINEL_CODE, dtype=torch.int8,
+                           device=device)
+        scales = torch.full(self.pool_shape()[:3], float("nan"), dtype=torch.float32,
+                            device=device)
+        return codes, codes.clone(), scales, scales.clone()
 
 
 def _randn_bf16(g: torch.Generator, shape) -> torch.Tensor:

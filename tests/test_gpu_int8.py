@@ -1,0 +1,145 @@
+"""CUDA INT8 KV path vs the oracle: the quantising cache write bit-exact
+(codes and scale bits, untouched rows keep their sentinels), and decode over
+the int8 pool within |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3 of
+the fp64 oracle over the same dequantised rows, for every split mode, at small
+sizes with ragged tails and at the full sizes of the workloads."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_decode_18_gb300 import binding as B
+from paged_kv_decode_18_gb300 import build as libbuild
+from paged_kv_decode_18_gb300 import workloads as W
+from tests.gpu_util import assert_attention_close, device
+from tests.pools import oracle_attention_i8, oracle_pools_i8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    libbuild.build()
+    B.load()
+
+
+class Int8Batch:
+    """A workload on the GPU with its int8 pool written by the CUDA quantising
+    cache write (history first, then the step's new tokens)."""
+
+    def __init__(self, w):
+        dev = device()
+        self.w, self.dev = w, dev
+        self.kc, self.vc, self.ks, self.vs = w.empty_pool_i8(dev)
+        if w.k_hist.shape[0]:
+            B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
+                                        self.kc, self.vc, self.ks, self.vs)
+        B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev),
+                                    self.kc, self.vc, self.ks, self.vs)
+        self.q = w.q.to(dev)
+        self.bt = w.block_tables.to(dev)
+        self.cl = w.context_lens.to(dev)
+
+    def pools(self):
+        return (self.kc.cpu().numpy(), self.vc.cpu().numpy(), self.ks.cpu().numpy(),
+                self.vs.cpu().numpy())
+
+    def decode(self, num_splits=0, with_lse=True):
+        out = torch.empty_like(self.q)
+        lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=self.dev) \
+            if with_lse else None
+        sh = B.shape_of(self.q, self.kc, self.bt)
+        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, num_splits), self.dev)
+        B.pa_decode_int8(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.cl,
+                         self.w.scale, out, lse, num_splits=num_splits, workspace=ws)
+        return out, lse
+
+
+def _same_pools(got, ref):
+    kc, vc, ks, vs = got
+    rkc, rvc, rks, rvs = ref
+    assert np.array_equal(kc, rkc) and np.array_equal(vc, rvc), "int8 codes differ"
+    # scales compared as bit patterns (NaN sentinels included)
+    assert np.array_equal(ks.view(np.uint32), rks.view(np.uint32)), "k scales differ"
+    assert np.array_equal(vs.view(np.uint32), rvs.view(np.uint32)), "v scales differ"
+
+
+@pytest.mark.parametrize("name,sizes", [("tiny", {}), ("engine", {}),
+                                        ("ragged", dict(num_seqs=40, max_context=700))])
+def test_int8_cache_write_bit_exact(name, sizes):
+    w = W.make(name, seed=21, **sizes)
+    db = Int8Batch(w)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    _same_pools(db.pools(), oracle_pools_i8(w))
+
+
+def test_int8_cache_write_zero_rows_and_padding():
+    w = W.make("tiny", seed=22)
+    dev = device()
+    kc, vc, ks, vs = w.empty_pool_i8(dev)
+    k = w.k_new.clone()
+    v = w.v_new.clone()
+    k[0] = 0  # whole rows of zeros -> codes 0, scale 0
+    v[1, 0] = 0
+    k[2, 1, 5] = 3e4  # an outlier in one row
+    slots = w.slot_new.clone()
+    slots[3] = -1  # padding: skipped
+    B.pa_reshape_and_cache_int8(k.to(dev), v.to(dev), slots.to(dev), kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    from oracle import oracle
+    rk, rv = np.full(w.pool_shape(), W.POOL_SENTINEL_CODE, np.int8), None
+    rv = rk.copy()
+    rks = np.full(w.pool_shape()[:3], np.nan, np.float32)
+    rvs = rks.copy()
+    oracle.reshape_and_cache_i8(k, v, slots, rk, rv, rks, rvs)
+    _same_pools((kc.cpu().numpy(), vc.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy()),
+                (rk, rv, rks, rvs))
+
+
+CASES = {
+    "tiny": ("tiny", {}),
+    "engine": ("engine", {}),
+    "ragged_small": ("ragged", dict(num_seqs=40, max_context=700)),
+    "long_small": ("long", dict(num_seqs=2, context=3000)),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_int8_decode_matches_oracle(case, num_splits):
+    name, sizes = CASES[case]
+    w = W.make(name, seed=23, **sizes)
+    db = Int8Batch(w)
+    out, lse = db.decode(num_splits)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention_i8(w)  # the oracle quantises its own pool
+    assert_attention_close(out, lse, ref, ref_lse, what=f"int8 {case} P={num_splits}")
+
+
+@pytest.mark.parametrize("name", ["ragged", "long"])
+def test_int8_decode_full_size(name):
+    # the full ragged (256 sequences up to 4096) and long (8 x 32k) batches:
+    # every row of the ragged batch, sampled rows of the long one
+    w = W.make(name, seed=24)
+    db = Int8Batch(w)
+    out, lse = db.decode(0)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention_i8(w)
+    assert_attention_close(out, lse, ref, ref_lse, what=f"int8 full {name}")
+    out_nl, _ = db.decode(0, with_lse=False)
+    assert torch.equal(out, out_nl)
+
+
+def test_int8_decode_close_to_bf16_decode():
+    # the same batch through both pool formats: the int8 answer stays near
+    # the bf16 one (quantisation error, not parity)
+    from tests.gpu_util import DeviceBatch
+    w = W.make("engine", seed=25)
+    out8, lse8 = Int8Batch(w).decode(0)
+    outb, lseb = DeviceBatch(w).decode(0)
+    torch.cuda.synchronize()
+    assert (out8.float() - outb.float()).abs().max().item() < 0.05
+    assert (lse8 - lseb).abs().max().item() < 0.05
