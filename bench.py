@@ -409,6 +409,74 @@ def run_secondary(args, dev, B):
         torch.cuda.empty_cache()
     res.update(run_secondary_varlen(args, dev, B, peak))
     res.update(run_secondary_int8(args, dev, B, peak))
+    res.update(run_secondary_cascade(args, dev, B, peak))
+    return res
+
+
+def unique_kv_bytes(w) -> int:
+    """KV bytes of the distinct physical rows a batch attends (a shared prefix
+    counted once), plus q / out / lse: the bytes a cascade decode must move."""
+    ctx = w.context_lens.to(torch.int64)
+    tokens = int(ctx.sum())
+    for seqs, t in w.meta.get("prefix_groups", []):
+        tokens -= t * (len(seqs) - 1)
+    rows = w.num_q_tokens
+    return (tokens * w.num_kv_heads * w.head_dim * 2 * 2 +
+            rows * w.num_q_heads * w.head_dim * 2 * 2 + rows * w.num_q_heads * 4)
+
+
+def run_secondary_cascade(args, dev, B, peak):
+    """Cascade (shared-prefix) decode against plain balanced decode on the
+    ragged batch (30% share a 512-token prefix) and on a shared-prompt batch
+    (128 sequences behind one 4096-token prompt)."""
+    from paged_kv_decode_18_gb300 import workloads as W
+
+    res = {}
+    for name, make in (("ragged", W.ragged), ("shared_prompt", W.shared_prompt)):
+        w = make(seed=args.seed)
+        kc, vc = w.empty_pool(dev)
+        B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
+        B.pa_reshape_and_cache(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), kc, vc)
+        q = w.q.to(dev)
+        bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        sh = B.shape_of(q, kc, bt)
+        sg, cu, mem, pl, mg, mp = W.cascade_groups(w)
+        sg, cu, mem, pl = sg.to(dev), cu.to(dev), mem.to(dev), pl.to(dev)
+        wsd = B.workspace(B.pa_decode_workspace_size(sh, 0), dev)
+        wsc = B.workspace(B.pa_decode_cascade_workspace_size(sh, pl.shape[0], mem.numel(), mg,
+                                                             mp), dev)
+        calls = {
+            "decode": lambda: B.pa_decode(q, kc, vc, bt, cl, w.scale, out, lse,  # noqa
+                                          num_splits=0, workspace=wsd),
+            "cascade": lambda: B.pa_decode_cascade(q, kc, vc, bt, cl, sg, cu, mem, pl, mg,  # noqa
+                                                   mp, w.scale, out, lse, workspace=wsc),
+        }
+        ub = unique_kv_bytes(w)
+        for kind, fn in calls.items():
+            fn()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+                fn()
+            for _ in range(5):
+                g.replay()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(30)]
+            torch.cuda.synchronize()
+            torch.cuda._sleep(1_000_000)
+            for a, b in evs:
+                a.record()
+                g.replay()
+                b.record()
+            torch.cuda.synchronize()
+            ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / 2
+            res[f"{name}_{kind}"] = {"call_ms": round(ms, 5), "unique_kv_bytes": ub,
+                                     "unique_gbs": round(ub / (ms / 1e3) / 1e9, 1),
+                                     "tokens_per_s": w.num_q_tokens / (ms / 1e3)}
+        del kc, vc
+        torch.cuda.empty_cache()
     return res
 
 

@@ -73,7 +73,7 @@ typedef enum pa_status {
 #define PA_DEVERR_SLOT_RANGE 0x1u    /* slot_mapping[t] >= num_blocks * block_size */
 #define PA_DEVERR_BLOCK_RANGE 0x2u   /* a used block_tables entry outside [0, num_blocks) */
 #define PA_DEVERR_CONTEXT_RANGE 0x4u /* context_len < 0 or > max_blocks_per_seq * block_size */
-#define PA_DEVERR_QLEN_RANGE 0x8u    /* q_len < 0, q_len > context_len, or cu_seqlens_q inconsistent */
+#define PA_DEVERR_QLEN_RANGE 0x8u    /* q_len < 0, q_len > context_len (causal, or context 0), or cu_seqlens_q inconsistent */
 #define PA_DEVERR_PIPE_TIMEOUT 0x10u /* an asynchronous copy did not land within its time limit */
 #define PA_DEVERR_PLAN_OVERFLOW 0x20u /* work list larger than the launch was sized for */
 
@@ -209,7 +209,8 @@ int pa_decode_static_scratch(const pa_bf16* q, const pa_bf16* k_cache, const pa_
  *   cu_seqlens_q  [S+1] int32, cu_seqlens_q[0] == 0,
  *                 cu_seqlens_q[S] == num_q_tokens, non-decreasing
  *   max_q_len     an upper bound of the q_lens (host value, sizes the launch)
- *   causal        1: query j sees keys 0 .. c - Lq + j; 0: it sees 0 .. c - 1
+ *   causal        1: query j sees keys 0 .. c - Lq + j (needs Lq <= c);
+ *                 0: it sees 0 .. c - 1 (any Lq when c > 0)
  *   out, lse      [num_q_tokens][Hq][D] bf16, [num_q_tokens][Hq] fp32 (lse may
  *                 be NULL)
  *   workspace     at least pa_decode_varlen_workspace_size(...) bytes,
@@ -276,6 +277,48 @@ int pa_decode_int8(const pa_bf16* q, const int8_t* k_cache, const int8_t* v_cach
 
 /* Workspace bytes for pa_decode_int8 with this shape and split choice. */
 size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_splits);
+
+/*
+ * pa_decode_cascade -- pa_decode (q_len 1, balanced) for a batch in which
+ * groups of sequences share the physical blocks of a prompt prefix (prefix
+ * caching: course README, "What to build in what order"; "S20 - The Complete
+ * Engine", "The conflicts": reference-counted shared blocks). Same result as
+ * pa_decode on the same q, pool, block_tables and context_lens (to fp32
+ * rounding): attention splits into the shared prefix, attended once per group
+ * by all its members together (non-causal multi-query tile on the tcgen05
+ * path, so the prefix's K/V are read once per group), and each sequence's own
+ * suffix (balanced decode), merged with the split-K formula.
+ *
+ *   seq_group      [S] int32: the group of sequence s, or -1
+ *   num_groups     G (host)
+ *   cu_group       [G+1] int32, cu_group[0] = 0: group g's members are
+ *                  group_members[cu_group[g] .. cu_group[g+1]-1]
+ *   group_members  [num_members] int32 sequence ids, increasing within a
+ *                  group, each sequence in at most one group
+ *   prefix_lens    [G] int32 prefix tokens of each group: > 0, a multiple of
+ *                  block_size, <= every member's context_len and <=
+ *                  max_prefix_len. Every member's first prefix_lens[g] /
+ *                  block_size block_tables entries are the same physical
+ *                  blocks (the library reads them from the first member).
+ *   num_members, max_group_size (>= every group's size), max_prefix_len
+ *                  (a multiple of block_size): host bounds that size the launch
+ *   workspace      pa_decode_cascade_workspace_size(...) bytes, 256-byte
+ *                  aligned, clobbered.
+ * A description that breaks these rules sets PA_DEVERR_QLEN_RANGE or
+ * PA_DEVERR_CONTEXT_RANGE; the output is then unspecified. Built for
+ * num_q_heads == 2 * num_kv_heads (as pa_decode).
+ */
+int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      const int32_t* seq_group, int num_groups, const int32_t* cu_group,
+                      const int32_t* group_members, const int32_t* prefix_lens,
+                      int num_members, int max_group_size, int max_prefix_len, float scale,
+                      pa_bf16* out, float* lse, const pa_shape* shape, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for pa_decode_cascade (0 if the arguments are invalid). */
+size_t pa_decode_cascade_workspace_size(const pa_shape* shape, int num_groups, int num_members,
+                                        int max_group_size, int max_prefix_len);
 
 /*
  * pa_splitk_reduce -- merge of split-K partial softmax results (course

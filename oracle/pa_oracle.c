@@ -308,7 +308,10 @@ static int paged_attention_core(const uint16_t *q, const uint16_t *k16, const ui
     for (int s = 0; s < num_seqs; ++s) {
         int c = context_lens[s];
         int lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
-        if (c < 0 || lq < 0 || lq > c || c > max_blocks_per_seq * block_size)
+        /* causal: the window cannot be longer than the context; non-causal
+           queries see the whole (non-empty) context */
+        if (c < 0 || lq < 0 || (lq > c && (causal || c == 0)) ||
+            c > max_blocks_per_seq * block_size)
             return ORACLE_ERR_RANGE;
         int nb = (c + block_size - 1) / block_size;
         for (int b = 0; b < nb; ++b) {

@@ -44,6 +44,8 @@ EXPORTED = (
     "pa_reshape_and_cache_int8",
     "pa_decode_int8",
     "pa_decode_int8_workspace_size",
+    "pa_decode_cascade",
+    "pa_decode_cascade_workspace_size",
     "pa_splitk_reduce",
     "pa_status_string",
     "pa_debug_read_error",
@@ -107,6 +109,11 @@ def load(path: str | None = None):
         lib.pa_decode_int8.argtypes = [V, V, V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
         lib.pa_decode_int8_workspace_size.restype = sz
         lib.pa_decode_int8_workspace_size.argtypes = [S, i32]
+        lib.pa_decode_cascade.restype = i32
+        lib.pa_decode_cascade.argtypes = [V, V, V, V, V, V, i32, V, V, V, i32, i32, i32, f32,
+                                          V, V, S, V, sz, V]
+        lib.pa_decode_cascade_workspace_size.restype = sz
+        lib.pa_decode_cascade_workspace_size.argtypes = [S, i32, i32, i32, i32]
         lib.pa_splitk_reduce.restype = i32
         lib.pa_splitk_reduce.argtypes = [V, V, i64, i32, i32, i32, V, V, V]
         lib.pa_status_string.restype = ctypes.c_char_p
@@ -230,6 +237,45 @@ def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_s
                                             _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                             _ptr(v_scale), ctypes.byref(sh), _stream(stream)),
            "pa_reshape_and_cache_int8")
+
+
+def pa_decode_cascade_workspace_size(shape: pa_shape, num_groups: int, num_members: int,
+                                     max_group_size: int, max_prefix_len: int) -> int:
+    return int(load().pa_decode_cascade_workspace_size(ctypes.byref(shape), int(num_groups),
+                                                       int(num_members), int(max_group_size),
+                                                       int(max_prefix_len)))
+
+
+def pa_decode_cascade(q, k_cache, v_cache, block_tables, context_lens, seq_group, cu_group,
+                      group_members, prefix_lens, max_group_size, max_prefix_len, scale, out,
+                      lse=None, workspace=None, stream=None) -> None:
+    """Decode with shared prefixes attended once per group (same result as
+    pa_decode)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(seq_group, "seq_group", torch.int32, 1)
+    _need(cu_group, "cu_group", torch.int32, 1)
+    _need(prefix_lens, "prefix_lens", torch.int32, 1)
+    if group_members.numel():
+        _need(group_members, "group_members", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    sh = shape_of(q, k_cache, block_tables)
+    G = prefix_lens.shape[0]
+    if cu_group.shape[0] != G + 1 or seq_group.shape[0] != sh.num_seqs:
+        raise ValueError("group description shapes do not match")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_cascade(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                    _ptr(context_lens), _ptr(seq_group), G, _ptr(cu_group),
+                                    _ptr(group_members) if group_members.numel() else None,
+                                    _ptr(prefix_lens), int(group_members.numel()),
+                                    int(max_group_size), int(max_prefix_len), float(scale),
+                                    _ptr(out), _ptr(lse), ctypes.byref(sh), _ptr(workspace),
+                                    ws_bytes, _stream(stream)), "pa_decode_cascade")
 
 
 def pa_decode_int8_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:

@@ -21,6 +21,7 @@ extern "C" int pa_debug_read_error(void* stream) {
   word |= pa::take_error_word_decode(st, &rc);
   word |= pa::take_error_word_varlen(st, &rc);
   word |= pa::take_error_word_prefill(st, &rc);
+  word |= pa::take_error_word_cascade(st, &rc);
   if (rc != PA_OK) return rc;
   return static_cast<int>(word);
 }

@@ -77,6 +77,11 @@ struct DecodeArgs {
   float* part_o;    // kBalanced: [NW*2][G][D]; kFixed: [S][Hq][P][D]
   float* part_lse;  // kBalanced: [NW*2][G];    kFixed: [S][Hq][P]
   int early;        // 1: plan and table reads may run before the previous grid ends
+  // fp32 row output (balanced mode only): when rows_o is set, finished rows go
+  // to rows_o[(row * rows_stride + rows_slot) * D] and rows_lse[row *
+  // rows_stride + rows_slot] (normalised o and lse, as one split-K partial)
+  // instead of out / lse
+  RowsOut rows;
 };
 
 // Write 8 dims (one lane's chunk) of one output row as bf16.
@@ -183,9 +188,16 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     for (int s = warp; s < S; s += NWARPS) {
       if (P.ctx[s] != 0) continue;
       for (int h = 0; h < Hq; ++h) {
-        uint2 z = make_uint2(0u, 0u);
-        *reinterpret_cast<uint2*>(a.out + ((size_t)s * Hq + h) * kHeadDim + lane * 4) = z;
-        if (a.lse && lane == 0) a.lse[(size_t)s * Hq + h] = neg_inf();
+        const size_t row = (size_t)s * Hq + h;
+        if (a.rows.o) {
+          const size_t r = row * a.rows.stride + a.rows.slot;
+          *reinterpret_cast<float4*>(a.rows.o + r * kHeadDim + lane * 4) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
+          if (lane == 0) a.rows.lse[r] = neg_inf();
+          continue;
+        }
+        *reinterpret_cast<uint2*>(a.out + row * kHeadDim + lane * 4) = make_uint2(0u, 0u);
+        if (a.lse && lane == 0) a.lse[row] = neg_inf();
       }
     }
   }
@@ -453,6 +465,10 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
         const int PS = a.num_splits;
         store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
         if ((lane & 15) == 0) a.part_lse[row * PS + fixed_p] = lse_own;
+      } else if (complete && a.rows.o) {
+        const size_t r = row * a.rows.stride + a.rows.slot;
+        store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
+        if ((lane & 15) == 0) a.rows.lse[r] = lse_own;
       } else if (complete) {
         store_out8(a.out + row * kHeadDim + od, o8, inv);
         if (a.lse && (lane & 15) == 0) a.lse[row] = lse_own;
@@ -480,7 +496,7 @@ __global__ void __launch_bounds__(256)
     decode_fixup_kernel(const int32_t* __restrict__ context_lens, int S, int Hkv, int max_blocks,
                         int num_workers, const float* __restrict__ part_o,
                         const float* __restrict__ part_lse, int Hq, uint16_t* __restrict__ out,
-                        float* __restrict__ lse) {
+                        float* __restrict__ lse, const RowsOut rows) {
   // the next grid in the stream may start its own preparation now; it waits
   // for this grid before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -566,6 +582,12 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int g = 0; g < kG; ++g) {
     const size_t row = (size_t)s * Hq + (size_t)h * kG + g;
+    if (rows.o) {
+      const size_t r = row * rows.stride + rows.slot;
+      *reinterpret_cast<float4*>(rows.o + r * kHeadDim + lane * 4) = acc[g];
+      if (lane == 0) rows.lse[r] = LSE[g];
+      continue;
+    }
     uint2 o;
     o.x = pack_bf2(acc[g].x, acc[g].y);
     o.y = pack_bf2(acc[g].z, acc[g].w);
@@ -751,12 +773,13 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
                 const float* k_scale, const float* v_scale, const int32_t* block_tables,
                 const int32_t* context_lens, float scale, pa_bf16* out, float* lse,
                 const pa_shape* shape, int num_splits, void* workspace, size_t workspace_bytes,
-                cudaStream_t st, int early) {
+                cudaStream_t st, int early, const RowsOut* rows = nullptr) {
   const bool q8 = k_scale != nullptr;
   int rc = check_decode_args(shape, num_splits);
   if (rc != PA_OK) return rc;
   if (shape->num_seqs == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || (!out && !rows))
+    return PA_ERR_ARG;
   if (q8 && !v_scale) return PA_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(block_tables, 4) || !aligned(context_lens, 4) || (lse && !aligned(lse, 4)) ||
@@ -790,6 +813,10 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   a.num_splits = g.P;
   a.num_workers = g.workers;
   a.early = early;
+  if (rows) {
+    if (g.mode != kBalanced || !rows->o || !rows->lse) return PA_ERR_ARG;
+    a.rows = *rows;
+  }
   char* ws = static_cast<char*>(workspace);
   a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
   a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
@@ -807,7 +834,7 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
     if (launch_dependent(decode_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32),
                          g.fixup_smem, st, context_lens, a.S, a.Hkv, a.max_blocks, g.workers,
                          (const float*)a.part_o, (const float*)a.part_lse, a.Hq, (uint16_t*)out,
-                         lse) != cudaSuccess)
+                         lse, a.rows) != cudaSuccess)
       return PA_ERR_CUDA;
   } else if (g.P > 1) {
     const int64_t nrh = (int64_t)a.S * a.Hq;
@@ -819,6 +846,15 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
 }
 
 }  // namespace
+
+int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, float scale,
+                const pa_shape* shape, const RowsOut& rows, void* workspace,
+                size_t workspace_bytes, cudaStream_t st) {
+  return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
+                     nullptr, nullptr, shape, 0, workspace, workspace_bytes, st, 0, &rows);
+}
+
 }  // namespace pa
 
 extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,

@@ -266,7 +266,10 @@ __device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scra
     if (varlen) {
       const int q0 = in.cu_seqlens_q[s];
       int lq = in.cu_seqlens_q[s + 1] - q0;
-      if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) {
+      // causal: a query window cannot be longer than its context; non-causal
+      // queries see the whole (non-empty) context whatever their number
+      if (lq < 0 || (lq > c && (in.causal || c == 0)) || q0 < 0 ||
+          (int64_t)q0 + lq > in.num_q_rows) {
         flag_error(PA_DEVERR_QLEN_RANGE);
         lq = 0;  // the sequence produces no rows
       }
@@ -303,7 +306,9 @@ __device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scra
       const int c = P.ctx[s];
       const int q0 = in.cu_seqlens_q[s];
       int lq = in.cu_seqlens_q[s + 1] - q0;
-      if (lq < 0 || lq > c || q0 < 0 || (int64_t)q0 + lq > in.num_q_rows) lq = 0;
+      if (lq < 0 || (lq > c && (in.causal || c == 0)) || q0 < 0 ||
+          (int64_t)q0 + lq > in.num_q_rows)
+        lq = 0;
       if (lq < in.min_lq || lq > in.max_lq) lq = 0;
       for (int p = p0; p < p1; ++p)
         P.pair_off[p] = in.Hkv * pair_tiles(c, lq, p - p0, in.qtile, in.causal, in.key_tile);

@@ -80,6 +80,23 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 bl
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// fp32 row output of an attention launch, as one slot of a split-K partial
+// layout: row r (= token * Hq + head) goes to o[(r * stride + slot) * D] and
+// lse[r * stride + slot] (normalised o, natural-log lse).
+struct RowsOut {
+  float* o = nullptr;
+  float* lse = nullptr;
+  int stride = 1;
+  int slot = 0;
+  int64_t tokens = 0;  // output tokens (rows / Hq); a mapped token outside is skipped
+};
+
+// Balanced decode (pa_decode with num_splits 0) writing fp32 rows (pa_decode.cu).
+int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, float scale,
+                const pa_shape* shape, const RowsOut& rows, void* workspace,
+                size_t workspace_bytes, cudaStream_t st);
+
 // ---------------------------------------------------------------------------
 // tensor maps (pa_varlen.cu)
 // ---------------------------------------------------------------------------
@@ -100,18 +117,24 @@ struct PrefillTcGeometry {
   size_t smem = 0, fixup_smem = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
 };
 
+// min_q_len: sequences with a shorter query window are left to another kernel.
 int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
-                        PrefillTcGeometry* g);
+                        PrefillTcGeometry* g, int min_q_len = kTcMinQLen);
+// rows / row_map (optional): write fp32 rows instead of out / lse, query
+// token i of q landing as token row_map[i] (row_map may be null: identity).
 int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf16* k_cache,
                       const pa_bf16* v_cache, const int32_t* block_tables,
                       const int32_t* context_lens, const int32_t* cu_seqlens_q,
                       int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
-                      const pa_shape* sh, void* workspace, cudaStream_t st);
+                      const pa_shape* sh, void* workspace, cudaStream_t st,
+                      int min_q_len = kTcMinQLen, const RowsOut* rows = nullptr,
+                      const int32_t* row_map = nullptr);
 
 // Each TU that owns kernels exposes the reader of its device error word.
 unsigned take_error_word_cache(cudaStream_t stream, int* rc);
 unsigned take_error_word_decode(cudaStream_t stream, int* rc);
 unsigned take_error_word_varlen(cudaStream_t stream, int* rc);
 unsigned take_error_word_prefill(cudaStream_t stream, int* rc);
+unsigned take_error_word_cascade(cudaStream_t stream, int* rc);
 
 }  // namespace pa

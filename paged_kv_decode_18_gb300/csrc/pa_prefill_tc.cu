@@ -80,7 +80,21 @@ struct TcArgs {
   int min_lq;
   float* part_o;    // [NW * 2][128 rows][128]
   float* part_lse;  // [NW * 2][128 rows]
+  RowsOut rows;     // fp32 row output instead of out / lse (rows.o set)
+  const int32_t* row_map;  // rows mode: query token i -> output token row_map[i]
 };
+
+// Output row (token * Hq + head) of query token qtok, head hd; -1 when the
+// row map sends it outside the output (flagged, not written).
+__device__ __forceinline__ int64_t out_row(const TcArgs& a, int64_t qtok, int hd) {
+  if (!a.row_map) return qtok * a.Hq + hd;
+  const int64_t t = a.row_map[qtok];
+  if (t < 0 || t >= a.rows.tokens) {
+    flag_error(PA_DEVERR_QLEN_RANGE);
+    return -1;
+  }
+  return t * a.Hq + hd;
+}
 
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
@@ -471,7 +485,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           o[j] = fmaf(__uint_as_float(u0[j]), c0, __uint_as_float(u1[j]) * c1);
-        if (pend_complete) {
+        if (pend_complete && a.rows.o) {
+          if (pend_valid) {
+            float4* dst = reinterpret_cast<float4*>(
+                a.rows.o + (pend_orow * a.rows.stride + a.rows.slot) * kHeadDim + d0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+        } else if (pend_complete) {
           if (pend_valid) {
             uint4* dst = reinterpret_cast<uint4*>(a.out + pend_orow * kHeadDim + d0);
 #pragma unroll
@@ -490,7 +512,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         }
       }
       if (hf == 0) {
-        if (pend_complete) {
+        if (pend_complete && a.rows.o) {
+          if (pend_valid) a.rows.lse[pend_orow * a.rows.stride + a.rows.slot] = lse_v;
+        } else if (pend_complete) {
           if (pend_valid && a.lse) a.lse[pend_orow] = lse_v;
         } else {
           a.part_lse[pend_slot * kRowsT + r] = lse_v;
@@ -627,8 +651,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         pend_m = m_ref;
         pend_l = l;
         pend_complete = (piece_b0 == 0) && (t.b == t.nt - 1);
-        pend_valid = valid;
-        pend_orow = ((int64_t)P.qstart[t.s] + tok) * a.Hq + (int64_t)t.h * G + r % G;
+        pend_orow = valid ? out_row(a, (int64_t)P.qstart[t.s] + tok, t.h * G + r % G) : 0;
+        pend_valid = valid && pend_orow >= 0;
         pend_slot = (size_t)w * 2 + (piece_first ? 0 : 1);
       }
       if (idx + 1 < R1) advance(P, S, Hkv, t);
@@ -729,7 +753,16 @@ __global__ void __launch_bounds__(kFixThreads)
 #pragma unroll
   for (int j = 0; j < 16; ++j) acc[j] *= inv;
   const float LSE = sum > 0.f ? m + lg2(sum) * kLn2 : neg_inf();
-  const int64_t orow = ((int64_t)q0 + tok) * a.Hq + (int64_t)job.h * a.G + r % a.G;
+  const int64_t orow = out_row(a, (int64_t)q0 + tok, job.h * a.G + r % a.G);
+  if (orow < 0) return;
+  if (a.rows.o) {
+    float4* dst = reinterpret_cast<float4*>(a.rows.o + (orow * a.rows.stride + a.rows.slot) * kHeadDim + d0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      dst[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+    if ((lane & 7) == 0) a.rows.lse[orow * a.rows.stride + a.rows.slot] = LSE;
+    return;
+  }
   uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kHeadDim + d0);
   dst[0] = make_uint4(cvt_bf16x2(acc[0], acc[1]), cvt_bf16x2(acc[2], acc[3]),
                       cvt_bf16x2(acc[4], acc[5]), cvt_bf16x2(acc[6], acc[7]));
@@ -759,11 +792,11 @@ size_t plan_bytes(int S, int npairs_cap) {
 }  // namespace
 
 int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
-                        PrefillTcGeometry* g) {
+                        PrefillTcGeometry* g, int min_q_len) {
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int G = sh->num_q_heads / sh->num_kv_heads;
-  if (G > kRowsT || kRowsT % G != 0 || max_q_len < kTcMinQLen) {
+  if (G > kRowsT || kRowsT % G != 0 || max_q_len < min_q_len || max_q_len < 1) {
     g->enabled = false;
     g->ws_bytes = 0;
     return PA_OK;
@@ -803,12 +836,13 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
                       const pa_bf16* v_cache, const int32_t* block_tables,
                       const int32_t* context_lens, const int32_t* cu_seqlens_q,
                       int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
-                      const pa_shape* sh, void* workspace, cudaStream_t st) {
+                      const pa_shape* sh, void* workspace, cudaStream_t st, int min_q_len,
+                      const RowsOut* rows, const int32_t* row_map) {
   const int G = sh->num_q_heads / sh->num_kv_heads;
   CUtensorMap tmq, tmk, tmv;
-  const int64_t rows = sh->num_blocks * sh->num_kv_heads * kBlock;
+  const int64_t pool_rows = sh->num_blocks * sh->num_kv_heads * kBlock;
   if (!make_q_map(&tmq, q, num_q_tokens, sh->num_q_heads, G, g.QTb) ||
-      !make_pool_map(&tmk, k_cache, rows) || !make_pool_map(&tmv, v_cache, rows))
+      !make_pool_map(&tmk, k_cache, pool_rows) || !make_pool_map(&tmv, v_cache, pool_rows))
     return PA_ERR_CUDA;
   TcArgs a;
   a.block_tables = block_tables;
@@ -828,7 +862,9 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
   a.causal = causal ? 1 : 0;
   a.npairs_cap = g.npairs_cap;
   a.num_workers = g.workers;
-  a.min_lq = kTcMinQLen;
+  a.min_lq = min_q_len;
+  if (rows) a.rows = *rows;
+  a.row_map = row_map;
   char* ws = static_cast<char*>(workspace);
   a.part_lse = reinterpret_cast<float*>(ws);
   a.part_o = reinterpret_cast<float*>(ws + g.ws_lse);

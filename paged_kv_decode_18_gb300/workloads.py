@@ -110,13 +110,15 @@ def build(name: str, seed: int, context_lens, q_lens, *, num_blocks: int | None 
           num_q_heads: int = NUM_Q_HEADS, num_kv_heads: int = NUM_KV_HEADS,
           head_dim: int = HEAD_DIM, block_size: int = BLOCK_SIZE,
           max_blocks_per_seq: int | None = None, scale: float | None = None,
-          meta: dict | None = None) -> Workload:
+          meta: dict | None = None, prefix_groups=()) -> Workload:
     """Build a workload from explicit per-sequence lengths.
 
     context_lens[s] counts all tokens of sequence s including its q_lens[s]
     new ones. Sequences listed in ``share_prefix_seqs`` use the same physical
     blocks for their first ``prefix_tokens`` positions (a refcounted prefix);
     their K/V there is one shared draw, written once (by the first sharer).
+    ``prefix_groups`` generalises this to several disjoint groups, a list of
+    (sequences, prefix_tokens); the single-group arguments are its first entry.
     ``outlier_frac`` of all key rows (token, KV head) are multiplied by
     ``outlier_gain`` before rounding to bf16.
     """
@@ -128,15 +130,23 @@ def build(name: str, seed: int, context_lens, q_lens, *, num_blocks: int | None 
     for c, l in zip(ctx, ql):
         assert 0 <= l <= c, (l, c)
     BS = block_size
-    sharers = sorted(set(int(s) for s in share_prefix_seqs))
-    if sharers:
-        assert prefix_tokens % BS == 0 and prefix_tokens > 0
-        for s in sharers:
+    groups = []  # (sorted sequences, prefix tokens)
+    legacy = sorted(set(int(s) for s in share_prefix_seqs))
+    if legacy:
+        groups.append((legacy, int(prefix_tokens)))
+    for seqs, tokens in prefix_groups:
+        groups.append((sorted(set(int(s) for s in seqs)), int(tokens)))
+    group_of = {}
+    for gi, (seqs, tokens) in enumerate(groups):
+        assert tokens % BS == 0 and tokens > 0 and seqs
+        for s in seqs:
+            assert s not in group_of, "prefix groups must be disjoint"
+            group_of[s] = gi
             # a sharer's own new tokens must land past the shared prefix
-            assert ctx[s] - ql[s] >= prefix_tokens, (s, ctx[s], ql[s])
-    prefix_blocks = prefix_tokens // BS if sharers else 0
+            assert ctx[s] - ql[s] >= tokens, (s, ctx[s], ql[s])
+    sharers = sorted(group_of)
     nblk = [(c + BS - 1) // BS for c in ctx]
-    needed = sum(nblk) - prefix_blocks * max(len(sharers) - 1, 0)
+    needed = sum(nblk) - sum((t // BS) * (len(ss) - 1) for ss, t in groups)
     if num_blocks is None:
         num_blocks = max(int(math.ceil(needed * pool_factor)), needed, 1)
     assert num_blocks >= needed, (num_blocks, needed)
@@ -147,12 +157,14 @@ def build(name: str, seed: int, context_lens, q_lens, *, num_blocks: int | None 
     perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
     tables = torch.full((S, max_blocks_per_seq), -1, dtype=torch.int32)
     cursor = 0
-    prefix_ids = perm[:prefix_blocks]
-    cursor += prefix_blocks
+    prefix_ids = []
+    for seqs, tokens in groups:
+        prefix_ids.append(perm[cursor:cursor + tokens // BS])
+        cursor += tokens // BS
     for s in range(S):
         row = []
-        if s in sharers:
-            row.extend(prefix_ids.tolist())
+        if s in group_of:
+            row.extend(prefix_ids[group_of[s]].tolist())
         k = nblk[s] - len(row)
         row.extend(perm[cursor:cursor + k].tolist())
         cursor += k
@@ -168,8 +180,11 @@ def build(name: str, seed: int, context_lens, q_lens, *, num_blocks: int | None 
     Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
     hist_lens = [c - l for c, l in zip(ctx, ql)]
     Th, Tq = sum(hist_lens), sum(ql)
-    prefix_k = _randn_bf16(g, (prefix_tokens, Hkv, D)) if sharers else None
-    prefix_v = _randn_bf16(g, (prefix_tokens, Hkv, D)) if sharers else None
+    prefix_kv = []
+    for seqs, tokens in groups:
+        pk = _randn_bf16(g, (tokens, Hkv, D))
+        pv = _randn_bf16(g, (tokens, Hkv, D))
+        prefix_kv.append((pk, pv))
     k_hist = _randn_bf16(g, (Th, Hkv, D))
     v_hist = _randn_bf16(g, (Th, Hkv, D))
     k_new = _randn_bf16(g, (Tq, Hkv, D))
@@ -179,18 +194,18 @@ def build(name: str, seed: int, context_lens, q_lens, *, num_blocks: int | None 
     slot_new = torch.empty(Tq, dtype=torch.int64)
     cu_hist = torch.zeros(S + 1, dtype=torch.int32)
     cu_q = torch.zeros(S + 1, dtype=torch.int32)
-    first_sharer = sharers[0] if sharers else -1
-    sharer_set = set(sharers)
     th = 0
     tq = 0
     for s in range(S):
         h = hist_lens[s]
         slot_hist[th:th + h] = slots_of(s, 0, h)
-        if s in sharer_set:
-            k_hist[th:th + prefix_tokens] = prefix_k
-            v_hist[th:th + prefix_tokens] = prefix_v
-            if s != first_sharer:
-                slot_hist[th:th + prefix_tokens] = -1  # the first sharer writes these
+        if s in group_of:
+            seqs, tokens = groups[group_of[s]]
+            pk, pv = prefix_kv[group_of[s]]
+            k_hist[th:th + tokens] = pk
+            v_hist[th:th + tokens] = pv
+            if s != seqs[0]:
+                slot_hist[th:th + tokens] = -1  # the group's first sequence writes these
         slot_new[tq:tq + ql[s]] = slots_of(s, h, h + ql[s])
         th += h
         tq += ql[s]
@@ -217,7 +232,9 @@ def build(name: str, seed: int, context_lens, q_lens, *, num_blocks: int | None 
         block_tables=tables, q=q, k_new=k_new, v_new=v_new, slot_new=slot_new,
         k_hist=k_hist, v_hist=v_hist, slot_hist=slot_hist, cu_hist=cu_hist,
         meta=dict(meta or {}, seed=int(seed), needed_blocks=int(needed),
-                  shared_prefix_seqs=len(sharers), prefix_tokens=int(prefix_tokens)))
+                  shared_prefix_seqs=len(sharers),
+                  prefix_tokens=int(groups[0][1]) if groups else 0,
+                  prefix_groups=[(list(ss), int(t)) for ss, t in groups]))
 
 
 # --------------------------------------------------------------------------
@@ -273,6 +290,19 @@ def long(seed: int = 0, num_seqs: int = 8, context: int = 32768,
                  outlier_frac=outlier_frac, meta={"config": "long-context split-K"})
 
 
+def shared_prompt(seed: int = 0, num_seqs: int = 128, prefix_tokens: int = 4096,
+                  lo: int = 1, hi: int = 512, pool_factor: float = 1.1) -> Workload:
+    """Decode batch behind one long shared prompt: every sequence holds the
+    same ``prefix_tokens`` (same physical blocks) plus a private suffix of
+    uniform length in [lo, hi] whose last token is the step's new one."""
+    g = torch.Generator().manual_seed(int(seed) * 7919 + 5)
+    suf = torch.randint(lo, hi + 1, (num_seqs,), generator=g).tolist()
+    ctx = [prefix_tokens + x for x in suf]
+    return build("shared_prompt", seed, ctx, [1] * num_seqs, pool_factor=pool_factor,
+                 prefix_groups=[(list(range(num_seqs)), prefix_tokens)],
+                 meta={"config": "shared-prompt decode (cascade)"})
+
+
 def mixed(seed: int = 0, num_verify: int = 48, verify_q: int = 5, lo: int = 256,
           hi: int = 8192, prefill_chunk: int = 512, prefill_offsets=(0, 1536),
           pool_factor: float = 1.1) -> Workload:
@@ -308,3 +338,25 @@ def random_unique_slots(num_tokens: int, num_blocks: int, block_size: int,
     """A fully random set of distinct slots (int64), for a scatter test."""
     g = torch.Generator().manual_seed(int(seed))
     return torch.randperm(num_blocks * block_size, generator=g)[:num_tokens].to(torch.int64)
+
+
+def cascade_groups(w: Workload):
+    """The prefix-sharing structure of a workload, as the cascade decode call
+    takes it: (seq_group [S], cu_group [G+1], group_members [M], prefix_lens [G])
+    int32 tensors (members in increasing order) plus the host bounds
+    (max_group_size, max_prefix_len)."""
+    groups = w.meta.get("prefix_groups", [])
+    S = w.num_seqs
+    seq_group = torch.full((S,), -1, dtype=torch.int32)
+    cu, members, plens = [0], [], []
+    for gi, (seqs, tokens) in enumerate(groups):
+        seqs = sorted(seqs)
+        for s in seqs:
+            seq_group[s] = gi
+        members.extend(seqs)
+        cu.append(len(members))
+        plens.append(tokens)
+    return (seq_group, torch.tensor(cu, dtype=torch.int32),
+            torch.tensor(members, dtype=torch.int32), torch.tensor(plens, dtype=torch.int32),
+            max((len(ss) for ss, _ in groups), default=0),
+            max((t for _, t in groups), default=0))
