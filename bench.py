@@ -671,26 +671,55 @@ def run_case(args, dev):
 
     libbuild.build()
     B.load()
-    w = W.make(args.case, seed=args.seed)
-    kc, vc = w.empty_pool(dev)
-    B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
+    if args.case == "prefill":  # the chunked-prefill part of the mixed batch
+        w = W.mixed(seed=args.seed, num_verify=0)
+    elif args.case == "ragged_int8":
+        w = W.ragged(seed=args.seed)
+    elif args.case == "shared_prompt":
+        w = W.shared_prompt(seed=args.seed)
+    else:
+        w = W.make(args.case, seed=args.seed)
+    int8 = args.case == "ragged_int8"
+    if int8:
+        kc, vc, ks, vs = w.empty_pool_i8(dev)
+        B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
+                                    kc, vc, ks, vs)
+    else:
+        kc, vc = w.empty_pool(dev)
+        B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
     k_new, v_new, slot_new = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
     q = w.q.to(dev)
     bt, cl, cu = w.block_tables.to(dev), w.context_lens.to(dev), w.cu_seqlens_q.to(dev)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
     sh = B.shape_of(q, kc, bt)
-    varlen = args.case == "mixed"
+    varlen = args.case in ("mixed", "prefill")
+    cascade = args.case == "shared_prompt"
     if varlen:
         ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, q.shape[0], w.max_q_len), dev)
+    elif int8:
+        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, args.splits), dev)
+    elif cascade:
+        sg, cg, mem, pl, mg, mp = W.cascade_groups(w)
+        sg, cg, mem, pl = sg.to(dev), cg.to(dev), mem.to(dev), pl.to(dev)
+        ws = B.workspace(B.pa_decode_cascade_workspace_size(sh, pl.shape[0], mem.numel(), mg,
+                                                            mp), dev)
     else:
         ws = B.workspace(B.pa_decode_workspace_size(sh, args.splits), dev)
 
     def step():
+        if int8:
+            B.pa_reshape_and_cache_int8(k_new, v_new, slot_new, kc, vc, ks, vs)
+            B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse,
+                             num_splits=args.splits, workspace=ws)
+            return
         B.pa_reshape_and_cache(k_new, v_new, slot_new, kc, vc)
         if varlen:
             B.pa_decode_varlen(q, kc, vc, bt, cl, cu, w.max_q_len, w.scale, out, lse,
                                causal=True, workspace=ws)
+        elif cascade:
+            B.pa_decode_cascade(q, kc, vc, bt, cl, sg, cg, mem, pl, mg, mp, w.scale, out, lse,
+                                workspace=ws)
         else:
             B.pa_decode(q, kc, vc, bt, cl, w.scale, out, lse, num_splits=args.splits,
                         workspace=ws)
@@ -723,7 +752,8 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["tiny", "engine", "ragged", "long", "mixed"],
+    ap.add_argument("--case", choices=["tiny", "engine", "ragged", "long", "mixed", "prefill",
+                                       "ragged_int8", "shared_prompt"],
                     help="time one workload with eager calls (for profiling), nothing else")
     ap.add_argument("--splits", type=int, default=0, help="num_splits for --case decode runs")
     args = ap.parse_args()

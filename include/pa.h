@@ -153,9 +153,12 @@ size_t pa_decode_workspace_size(const pa_shape* shape, int num_splits);
  * layouts, results and workspace (pa_decode_workspace_size(shape, 0)) as the
  * two calls. The decode grid is queued as a programmatic dependent of the
  * cache-write grid and prepares its work (reading context_lens and
- * block_tables) while the write runs; it reads the pool only after the write
- * has finished. So context_lens and block_tables must not alias k_new, v_new,
- * slot_mapping or the pool.
+ * block_tables) while the write runs, then streams every tile of the pool
+ * except the last block of each (sequence, KV head) at once; a last block is
+ * copied only after the write has finished. So: each new row must land in
+ * the block that holds its sequence's last position (context_lens[s] - 1:
+ * the decode step's own token), and context_lens and block_tables must not
+ * alias k_new, v_new, slot_mapping or the pool.
  */
 int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new, const int64_t* slot_mapping,
                      int64_t num_new_tokens, const pa_bf16* q, pa_bf16* k_cache,

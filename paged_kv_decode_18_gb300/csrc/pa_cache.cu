@@ -101,6 +101,30 @@ __global__ void reshape_and_cache_int8_kernel(const uint2* __restrict__ k,
 
 }  // namespace
 
+int launch_cache_write(const pa_bf16* k, const pa_bf16* v, const int64_t* slot_mapping,
+                       int64_t num_tokens, pa_bf16* k_cache, pa_bf16* v_cache,
+                       const pa_shape* shape, cudaStream_t st) {
+  int rc = check_shape_common(shape);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_ARG;
+  const int64_t total = num_tokens * shape->num_kv_heads * kChunksPerRow;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 0x7fffffff) return PA_ERR_ARG;
+  if (launch_dependent(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads), 0, st,
+                       reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
+                       slot_mapping, total, shape->num_kv_heads,
+                       shape->num_blocks * shape->block_size, reinterpret_cast<uint4*>(k_cache),
+                       reinterpret_cast<uint4*>(v_cache)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 unsigned take_error_word_cache(cudaStream_t stream, int* rc) {
   unsigned v = 0, zero = 0;
   if (cudaStreamSynchronize(stream) != cudaSuccess ||
@@ -120,26 +144,8 @@ extern "C" int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v,
                                     const int64_t* slot_mapping, int64_t num_tokens,
                                     pa_bf16* k_cache, pa_bf16* v_cache, const pa_shape* shape,
                                     void* stream) {
-  int rc = check_shape_common(shape);
-  if (rc != PA_OK) return rc;
-  if (num_tokens < 0) return PA_ERR_ARG;
-  if (num_tokens == 0) return PA_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
-  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(slot_mapping, 8))
-    return PA_ERR_ARG;
-  const int64_t total = num_tokens * shape->num_kv_heads * kChunksPerRow;
-  const int threads = 256;
-  const int64_t blocks = (total + threads - 1) / threads;
-  if (blocks > 0x7fffffff) return PA_ERR_ARG;
-  if (launch_dependent(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(threads), 0,
-                       static_cast<cudaStream_t>(stream), reinterpret_cast<const uint4*>(k),
-                       reinterpret_cast<const uint4*>(v), slot_mapping, total,
-                       shape->num_kv_heads, shape->num_blocks * shape->block_size,
-                       reinterpret_cast<uint4*>(k_cache),
-                       reinterpret_cast<uint4*>(v_cache)) != cudaSuccess)
-    return PA_ERR_CUDA;
-  return PA_OK;
+  return launch_cache_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, shape,
+                            static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v,

@@ -99,6 +99,86 @@ __device__ __forceinline__ void store_f8(float* dst, const float (&v)[8], float 
   reinterpret_cast<float4*>(dst)[1] = make_float4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
 }
 
+// Merge the pieces of one cut (sequence, KV head) segment -- the a7 formula
+// over workers w-1 .. job.last -- and write its two output rows. One warp.
+// Partials are read through L2 (ld.global.cg): other SMs wrote them.
+__device__ __forceinline__ void merge_segment(const MergeJob& job, int w, int lane,
+                                              const float* __restrict__ part_o,
+                                              const float* __restrict__ part_lse, int Hq,
+                                              uint16_t* __restrict__ out,
+                                              float* __restrict__ lse, const RowsOut& rows) {
+  const int s = job.s, h = job.h, last = job.last, slot_prev = job.slot_prev;
+  const int npieces = last - w + 2;  // workers w-1 .. last
+  float4 acc[kG];
+  for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // each round handles 32 pieces: lane i holds piece i's lse values while the
+  // partial vectors of the round are loaded at the same time
+  float mx[kG] = {neg_inf(), neg_inf()}, sum[kG] = {0.f, 0.f};
+  for (int i0 = 0; i0 < npieces; i0 += 32) {
+    const int n = min(32, npieces - i0);
+    float li[kG] = {neg_inf(), neg_inf()};
+    if (lane < n) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(part_lse + ((size_t)(w - 1 + i0 + lane) * 2 + (i0 + lane == 0 ? slot_prev : 0)) * kG));
+      li[0] = v.x;
+      li[1] = v.y;
+    }
+    float m[kG], e[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      m[g] = li[g];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(kFull, m[g], o));
+      m[g] = fmaxf(m[g], mx[g]);
+      // rescale what earlier rounds accumulated to the new maximum
+      const float r = ex2((mx[g] - m[g]) * kLog2e);
+      sum[g] *= r;
+      acc[g].x *= r; acc[g].y *= r; acc[g].z *= r; acc[g].w *= r;
+      e[g] = ex2((li[g] - m[g]) * kLog2e);  // unnormalised weight of piece lane
+      float t = e[g];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+      sum[g] += t;
+      mx[g] = m[g];
+    }
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const size_t slot = (size_t)(w - 1 + i0 + j) * 2 + (i0 + j == 0 ? slot_prev : 0);
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        const float wt = __shfl_sync(kFull, e[g], j);
+        const float4 o =
+            __ldcg(reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4));
+        acc[g].x = fmaf(wt, o.x, acc[g].x);
+        acc[g].y = fmaf(wt, o.y, acc[g].y);
+        acc[g].z = fmaf(wt, o.z, acc[g].z);
+        acc[g].w = fmaf(wt, o.w, acc[g].w);
+      }
+    }
+  }
+  float LSE[kG];
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
+    const float inv = 1.f / sum[g];
+    acc[g].x *= inv; acc[g].y *= inv; acc[g].z *= inv; acc[g].w *= inv;
+  }
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    const size_t row = (size_t)s * Hq + (size_t)h * kG + g;
+    if (rows.o) {
+      const size_t r = row * rows.stride + rows.slot;
+      *reinterpret_cast<float4*>(rows.o + r * kHeadDim + lane * 4) = acc[g];
+      if (lane == 0) rows.lse[r] = LSE[g];
+      continue;
+    }
+    uint2 o;
+    o.x = pack_bf2(acc[g].x, acc[g].y);
+    o.y = pack_bf2(acc[g].z, acc[g].w);
+    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane * 4) = o;
+    if (lse && lane == 0) lse[row] = LSE[g];
+  }
+}
+
 // Four signed bytes -> two float pairs, exactly: the byte (biased by 128)
 // becomes the low mantissa bits of 2^23, one packed subtraction removes both.
 __device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& lo, float2& hi) {
@@ -131,7 +211,7 @@ __device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)
 }
 
 template <int NWARPS, int NSTAGE, bool Q8>
-__global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const DecodeArgs a) {
   using L = WarpLayout<NSTAGE, Q8>;
   using F = KvFormat<Q8>;
   constexpr int kStageBytes = F::kStage;
@@ -156,9 +236,12 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   // This grid is launched as a programmatic dependent of the previous one on
   // the stream. By default it waits for that grid right here, before reading
   // anything. With `early` (used only behind this library's own cache-write
-  // kernel, which writes nothing but the pool) the plan and the block-table
-  // window are prepared first and the wait sits just before the first copy
-  // out of the pool.
+  // kernel, which writes nothing but the step's new rows, each in the last
+  // block of its sequence's context) the plan and the block-table window are
+  // prepared at once and every tile but a segment's last streams in while the
+  // write runs: a warp waits for the write only before it copies the last
+  // tile of a (sequence, KV head). Thread 0 of CTA 0 also waits once, so
+  // that this grid never completes before the write.
   if (!a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   PlanInputs in;
   in.context_lens = a.context_lens;
@@ -171,6 +254,11 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
   in.npairs_cap = S;
   in.num_q_rows = S;
   build_plan(in, P, scratch);  // ends with __syncthreads: barrier inits visible too
+  bool waited = !a.early;
+  if (a.early && blockIdx.x == 0 && threadIdx.x == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    waited = true;
+  }
   // the merge grid that follows may be scheduled from now on (it waits for
   // this grid to finish before it reads anything)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -263,6 +351,10 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
         flag_error(PA_DEVERR_BLOCK_RANGE);
         phys = 0;
       }
+      if (!waited && pp.b == pp.nt - 1) {  // the tile that holds the new row
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+      }
       unsigned char* st = wbuf + stage * kStageBytes;
       const uint32_t bar = smem_addr(&bars[stage]);
       fence_proxy_async_smem();
@@ -288,7 +380,6 @@ __global__ void __launch_bounds__(NWARPS * 32) paged_decode_kernel(const DecodeA
     }
   };
 
-  if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
 
   // ---- consumer -------------------------------------------------------------
@@ -524,76 +615,7 @@ __global__ void __launch_bounds__(256)
   const MergeJob job = merge_job(P, S, Hkv, w, W, nw);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!job.valid) return;
-  const int s = job.s, h = job.h, last = job.last, slot_prev = job.slot_prev;
-  const int npieces = last - w + 2;  // workers w-1 .. last
-  float4 acc[kG];
-  for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // each round handles 32 pieces: lane i holds piece i's lse values while the
-  // partial vectors of the round are loaded at the same time
-  float mx[kG] = {neg_inf(), neg_inf()}, sum[kG] = {0.f, 0.f};
-  for (int i0 = 0; i0 < npieces; i0 += 32) {
-    const int n = min(32, npieces - i0);
-    float li[kG] = {neg_inf(), neg_inf()};
-    if (lane < n) {
-      const float2 v = *reinterpret_cast<const float2*>(part_lse + ((size_t)(w - 1 + i0 + lane) * 2 + (i0 + lane == 0 ? slot_prev : 0)) * kG);
-      li[0] = v.x;
-      li[1] = v.y;
-    }
-    float m[kG], e[kG];
-#pragma unroll
-    for (int g = 0; g < kG; ++g) {
-      m[g] = li[g];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(kFull, m[g], o));
-      m[g] = fmaxf(m[g], mx[g]);
-      // rescale what earlier rounds accumulated to the new maximum
-      const float r = ex2((mx[g] - m[g]) * kLog2e);
-      sum[g] *= r;
-      acc[g].x *= r; acc[g].y *= r; acc[g].z *= r; acc[g].w *= r;
-      e[g] = ex2((li[g] - m[g]) * kLog2e);  // unnormalised weight of piece lane
-      float t = e[g];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
-      sum[g] += t;
-      mx[g] = m[g];
-    }
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
-      const size_t slot = (size_t)(w - 1 + i0 + j) * 2 + (i0 + j == 0 ? slot_prev : 0);
-#pragma unroll
-      for (int g = 0; g < kG; ++g) {
-        const float wt = __shfl_sync(kFull, e[g], j);
-        const float4 o =
-            *reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4);
-        acc[g].x = fmaf(wt, o.x, acc[g].x);
-        acc[g].y = fmaf(wt, o.y, acc[g].y);
-        acc[g].z = fmaf(wt, o.z, acc[g].z);
-        acc[g].w = fmaf(wt, o.w, acc[g].w);
-      }
-    }
-  }
-  float LSE[kG];
-#pragma unroll
-  for (int g = 0; g < kG; ++g) {
-    LSE[g] = mx[g] + lg2(sum[g]) * kLn2;
-    const float inv = 1.f / sum[g];
-    acc[g].x *= inv; acc[g].y *= inv; acc[g].z *= inv; acc[g].w *= inv;
-  }
-#pragma unroll
-  for (int g = 0; g < kG; ++g) {
-    const size_t row = (size_t)s * Hq + (size_t)h * kG + g;
-    if (rows.o) {
-      const size_t r = row * rows.stride + rows.slot;
-      *reinterpret_cast<float4*>(rows.o + r * kHeadDim + lane * 4) = acc[g];
-      if (lane == 0) rows.lse[r] = LSE[g];
-      continue;
-    }
-    uint2 o;
-    o.x = pack_bf2(acc[g].x, acc[g].y);
-    o.y = pack_bf2(acc[g].z, acc[g].w);
-    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane * 4) = o;
-    if (lse && lane == 0) lse[row] = LSE[g];
-  }
+  merge_segment(job, w, lane, part_o, part_lse, Hq, out, lse, rows);
 }
 
 // Split-K merge over a regular [rows][heads][P][D] partial layout: one warp
@@ -904,7 +926,8 @@ extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
                             stream);
   if (rc != PA_OK) return rc;
   // with new tokens, the cache write ran just before: the decode prologue
-  // (which reads only context_lens and block_tables) may overlap it
+  // (which reads only context_lens and block_tables) and every tile but the
+  // segments' last ones may overlap it
   return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
                      out, lse, shape, 0, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), num_new_tokens > 0 ? 1 : 0);

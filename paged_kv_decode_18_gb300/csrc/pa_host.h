@@ -91,6 +91,11 @@ struct RowsOut {
   int64_t tokens = 0;  // output tokens (rows / Hq); a mapped token outside is skipped
 };
 
+// Slot-mapped cache write (pa_cache.cu), as pa_reshape_and_cache.
+int launch_cache_write(const pa_bf16* k, const pa_bf16* v, const int64_t* slot_mapping,
+                       int64_t num_tokens, pa_bf16* k_cache, pa_bf16* v_cache,
+                       const pa_shape* shape, cudaStream_t st);
+
 // Balanced decode (pa_decode with num_splits 0) writing fp32 rows (pa_decode.cu).
 int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
                 const int32_t* block_tables, const int32_t* context_lens, float scale,
