@@ -477,7 +477,7 @@ __global__ void varlen_fixup_kernel(const int* __restrict__ desc, const float* _
 // host side
 // ---------------------------------------------------------------------------
 constexpr int kWarps = 6;
-constexpr int kStages = 2;
+constexpr int kStages = 3;  // one CTA per SM: 6 warps x 3 stages of 8 KB (best of a warps x stages sweep)
 
 struct VarlenGeometry {
   int grid = 0, workers = 0, npairs_cap = 0;
