@@ -355,6 +355,18 @@ const char* pa_status_string(int status);
  */
 int pa_debug_read_error(void* stream);
 
+/*
+ * pa_debug_inject_missing_copy -- failure-detection test hook. The next
+ * decode launch (pa_decode, pa_append_decode, pa_decode_int8 or
+ * pa_decode_static_scratch) on this host thread leaves out the copy of flat
+ * tile `flat_tile` of its work list (0 = the first (sequence 0, KV head 0,
+ * block 0) tile), so the warp that waits for it runs into its bounded wait
+ * (2 s), sets PA_DEVERR_PIPE_TIMEOUT and returns; the kernel exits, nothing
+ * traps and the context stays usable (that call's output is unspecified).
+ * A negative value clears a pending injection. Returns PA_OK.
+ */
+int pa_debug_inject_missing_copy(int flat_tile);
+
 /* Library version string, e.g. "pagedattn 0.1 sm_103a". */
 const char* pa_version(void);
 

@@ -49,6 +49,7 @@ EXPORTED = (
     "pa_splitk_reduce",
     "pa_status_string",
     "pa_debug_read_error",
+    "pa_debug_inject_missing_copy",
     "pa_version",
 )
 
@@ -120,6 +121,8 @@ def load(path: str | None = None):
         lib.pa_status_string.argtypes = [i32]
         lib.pa_debug_read_error.restype = i32
         lib.pa_debug_read_error.argtypes = [V]
+        lib.pa_debug_inject_missing_copy.restype = i32
+        lib.pa_debug_inject_missing_copy.argtypes = [i32]
         lib.pa_version.restype = ctypes.c_char_p
         lib.pa_version.argtypes = []
         _lib = lib
@@ -190,6 +193,12 @@ def pa_debug_read_error(stream=None) -> int:
     if rc < 0:
         raise PAError(rc, "pa_debug_read_error")
     return rc
+
+
+def pa_debug_inject_missing_copy(flat_tile: int) -> None:
+    """Failure-detection hook: the next decode launch leaves out the copy of
+    one tile, so its bounded wait expires and flags PA_DEVERR_PIPE_TIMEOUT."""
+    _check(load().pa_debug_inject_missing_copy(int(flat_tile)), "pa_debug_inject_missing_copy")
 
 
 def pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:

@@ -144,6 +144,7 @@ extern "C" int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v,
                                     const int64_t* slot_mapping, int64_t num_tokens,
                                     pa_bf16* k_cache, pa_bf16* v_cache, const pa_shape* shape,
                                     void* stream) {
+  pa::NvtxRange nvtx_range("pa_reshape_and_cache");
   return launch_cache_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, shape,
                             static_cast<cudaStream_t>(stream));
 }
@@ -152,6 +153,7 @@ extern "C" int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v,
                                          const int64_t* slot_mapping, int64_t num_tokens,
                                          int8_t* k_cache, int8_t* v_cache, float* k_scale,
                                          float* v_scale, const pa_shape* shape, void* stream) {
+  pa::NvtxRange nvtx_range("pa_reshape_and_cache_int8");
   int rc = check_shape_common(shape);
   if (rc != PA_OK) return rc;
   if (num_tokens < 0) return PA_ERR_ARG;

@@ -218,6 +218,7 @@ extern "C" int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache,
                                  int num_members, int max_group_size, int max_prefix_len,
                                  float scale, pa_bf16* out, float* lse, const pa_shape* shape,
                                  void* workspace, size_t workspace_bytes, void* stream) {
+  pa::NvtxRange nvtx_range("pa_decode_cascade");
   int rc = check_shape_common(shape);
   if (rc != PA_OK) return rc;
   const int S = shape->num_seqs;

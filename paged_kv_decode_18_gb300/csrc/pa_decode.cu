@@ -82,6 +82,7 @@ struct DecodeArgs {
   // rows_stride + rows_slot] (normalised o and lse, as one split-K partial)
   // instead of out / lse
   RowsOut rows;
+  int skip_copy;    // failure-detection hook: flat tile whose copy is left out (-1: none)
 };
 
 // Write 8 dims (one lane's chunk) of one output row as bf16.
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const Deco
   auto issue = [&](int stage) {
     int phys = __shfl_sync(kFull, phys_cur, pidx - wbase);
     const bool first = (pidx == R0) || (pp.b == 0);
-    if (lane == 0) {
+    if (lane == 0 && pidx != a.skip_copy) {
       if (phys < 0 || (int64_t)phys >= a.num_blocks) {
         flag_error(PA_DEVERR_BLOCK_RANGE);
         phys = 0;
@@ -788,6 +789,10 @@ extern "C" size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_s
 namespace pa {
 namespace {
 
+// Failure-detection hook (pa_debug_inject_missing_copy): consumed by the next
+// decode launch of this host thread.
+thread_local int g_inject_missing_copy = -1;
+
 // Validate, size and launch the decode grid and its merge. `early`: see the
 // kernel (only pa_append_decode sets it).
 // k_scale / v_scale non-null selects the int8 format.
@@ -835,6 +840,8 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   a.num_splits = g.P;
   a.num_workers = g.workers;
   a.early = early;
+  a.skip_copy = g_inject_missing_copy;
+  g_inject_missing_copy = -1;
   if (rows) {
     if (g.mode != kBalanced || !rows->o || !rows->lse) return PA_ERR_ARG;
     a.rows = *rows;
@@ -883,6 +890,7 @@ extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
                          const int32_t* block_tables, const int32_t* context_lens, float scale,
                          pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
                          void* workspace, size_t workspace_bytes, void* stream) {
+  pa::NvtxRange nvtx_range("pa_decode");
   return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
                      out, lse, shape, num_splits, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), 0);
@@ -894,6 +902,7 @@ extern "C" int pa_decode_int8(const pa_bf16* q, const int8_t* k_cache, const int
                               float scale, pa_bf16* out, float* lse, const pa_shape* shape,
                               int num_splits, void* workspace, size_t workspace_bytes,
                               void* stream) {
+  pa::NvtxRange nvtx_range("pa_decode_int8");
   if (!k_scale || !v_scale) return PA_ERR_ARG;
   return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
                      out, lse, shape, num_splits, workspace, workspace_bytes,
@@ -906,6 +915,7 @@ extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
                                 const int32_t* block_tables, const int32_t* context_lens,
                                 float scale, pa_bf16* out, float* lse, const pa_shape* shape,
                                 void* workspace, size_t workspace_bytes, void* stream) {
+  pa::NvtxRange nvtx_range("pa_append_decode");
   // check everything first so that a failing call enqueues nothing
   int rc = check_decode_args(shape, 0);
   if (rc != PA_OK) return rc;
@@ -936,6 +946,7 @@ extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
 extern "C" int pa_splitk_reduce(const float* part_out, const float* part_lse, int64_t num_rows,
                                 int num_heads, int num_splits, int head_dim, pa_bf16* out,
                                 float* lse, void* stream) {
+  pa::NvtxRange nvtx_range("pa_splitk_reduce");
   if (num_rows < 0 || num_heads <= 0 || num_splits <= 0 || head_dim <= 0) return PA_ERR_ARG;
   if (head_dim % 4 != 0 || head_dim > 1024) return PA_ERR_UNSUPPORTED;
   if (num_rows == 0) return PA_OK;
@@ -998,6 +1009,7 @@ extern "C" int pa_decode_static_scratch(const pa_bf16* q, const pa_bf16* k_cache
                                         const pa_bf16* v_cache, const int32_t* block_tables,
                                         const int32_t* context_lens, float scale, pa_bf16* out,
                                         float* lse, const pa_shape* shape, void* stream) {
+  pa::NvtxRange nvtx_range("pa_decode_static_scratch");
   int rc = check_decode_args(shape, 0);
   if (rc != PA_OK) return rc;
   if (shape->num_seqs == 0) return PA_OK;
@@ -1010,4 +1022,9 @@ extern "C" int pa_decode_static_scratch(const pa_bf16* q, const pa_bf16* k_cache
   if (scratch == nullptr) return rc;
   return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape, 0,
                    scratch, kStaticScratchBytes, stream);
+}
+
+extern "C" int pa_debug_inject_missing_copy(int flat_tile) {
+  pa::g_inject_missing_copy = flat_tile < 0 ? -1 : flat_tile;
+  return PA_OK;
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -61,6 +62,15 @@ inline int check_shape_common(const pa_shape* s) {
   if (s->num_blocks * s->num_kv_heads * s->block_size >= (int64_t(1) << 40)) return PA_ERR_ARG;
   return PA_OK;
 }
+
+// A named NVTX range around a C-ABI call (visible in Nsight timelines; a
+// no-op when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Launch a kernel as a programmatic dependent of the previous grid on the
 // stream (it may start before that grid ends and waits inside).

@@ -591,6 +591,7 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
                                 int max_q_len, int causal, float scale, pa_bf16* out, float* lse,
                                 const pa_shape* shape, void* workspace, size_t workspace_bytes,
                                 void* stream) {
+  pa::NvtxRange nvtx_range("pa_decode_varlen");
   int rc = check_varlen_args(shape, num_q_tokens, max_q_len);
   if (rc != PA_OK) return rc;
   if (shape->num_seqs == 0 || num_q_tokens == 0) return PA_OK;
