@@ -158,17 +158,23 @@ __global__ void cascade_prep_kernel(const uint4* __restrict__ q, const int32_t* 
       if (s >= 0 && s < S) id = block_tables[(int64_t)s * max_blocks + b];
     }
     prefix_bt[i] = id;
-    if (b == 0) {
-      if (m0 < 0 || m1 < m0 || m1 > num_members || prefix_lens[g] <= 0) {
-        flag_error(PA_DEVERR_QLEN_RANGE);
-      }
-      for (int m = m0; m < m1 && m < num_members; ++m) {
-        const int s = group_members[m];
-        if (s < 0 || s >= S || seq_group[s] != g ||
-            (m > m0 && group_members[m - 1] >= s))  // listed once, in increasing order
-          flag_error(PA_DEVERR_QLEN_RANGE);
-      }
+    if (b == 0 && (m0 < 0 || m1 < m0 || m1 > num_members || prefix_lens[g] <= 0))
+      flag_error(PA_DEVERR_QLEN_RANGE);
+  }
+  // every listed member belongs to the group whose range holds it, once, in
+  // increasing order (one thread per member; its group by binary search)
+  for (int64_t m = tid; m < num_members; m += nth) {
+    int lo = 0, hi = num_groups - 1, g = -1;
+    while (lo <= hi) {  // the group g with cu_group[g] <= m < cu_group[g + 1]
+      const int mid = (lo + hi) >> 1;
+      if (cu_group[mid + 1] <= m) lo = mid + 1;
+      else if (cu_group[mid] > m) hi = mid - 1;
+      else { g = mid; break; }
     }
+    const int s = group_members[m];
+    if (g < 0 || s < 0 || s >= S || seq_group[s] != g ||
+        (m > cu_group[g] && group_members[m - 1] >= s))
+      flag_error(PA_DEVERR_QLEN_RANGE);
   }
   // empty prefix partial (0, -inf) for every sequence in no group
   const int per_row = kHeadDim / 4;
