@@ -33,6 +33,8 @@ struct CascadeLayout {
   PrefillTcGeometry tg;
   pa_shape tc_shape{}, suffix_shape{};
   size_t dec_ws_bytes = 0;
+  int tc_ctas = 0;      // SMs given to the prefix half
+  int suffix_sms = 0;   // SMs the suffix half's grid is sized for (0: all)
 };
 
 int cascade_layout(const pa_shape* sh, int num_groups, int num_members, int max_group_size,
@@ -59,7 +61,22 @@ int cascade_layout(const pa_shape* sh, int num_groups, int num_members, int max_
   L->tc_shape.num_seqs = num_groups;
   L->tc_shape.max_blocks_per_seq = max_prefix_blocks;
   if (num_groups > 0 && num_members > 0 && max_prefix_blocks > 0) {
-    const int rc = prefill_tc_geometry(&L->tc_shape, num_members, max_group_size, &L->tg, 1);
+    // The two halves run side by side: the prefix half on tc_ctas SMs (about
+    // 12 of its 128 x 128 tiles per CTA, from an upper bound of its tile
+    // count: the best of a sweep of 4..24 on a shared-prompt batch), the
+    // suffix half on the others.
+    DeviceInfo dev;
+    if (!current_device_info(&dev)) return PA_ERR_CUDA;
+    const int G = sh->num_q_heads / sh->num_kv_heads;
+    const int qtb = 128 / (G > 0 ? G : 1);
+    const int64_t qtiles = (num_members + qtb - 1) / qtb + num_groups;
+    const int64_t tiles = qtiles * sh->num_kv_heads * ((max_prefix_len + 127) / 128);
+    int64_t want = (tiles + 11) / 12;
+    const int64_t cap = dev.num_sms / 2;
+    L->tc_ctas = (int)(want < 8 ? 8 : (want > cap ? cap : want));
+    L->suffix_sms = dev.num_sms - L->tc_ctas;
+    const int rc = prefill_tc_geometry(&L->tc_shape, num_members, max_group_size, &L->tg, 1,
+                                       L->tc_ctas);
     if (rc != PA_OK) return rc;
     if (!L->tg.enabled) return PA_ERR_UNSUPPORTED;
   } else {
@@ -67,7 +84,7 @@ int cascade_layout(const pa_shape* sh, int num_groups, int num_members, int max_
   }
   L->tc_ws = take(L->tg.enabled ? L->tg.ws_bytes : 0);
   L->suffix_shape = *sh;
-  L->dec_ws_bytes = S > 0 ? pa_decode_workspace_size(sh, 0) : 0;
+  L->dec_ws_bytes = S > 0 ? decode_rows_workspace_size(sh, L->suffix_sms) : 0;
   if (S > 0 && L->dec_ws_bytes == 0) return PA_ERR_ARG;
   L->dec_ws = take(L->dec_ws_bytes);
   L->total = off;
@@ -266,17 +283,31 @@ extern "C" int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache,
   prefix_rows.stride = 2;
   prefix_rows.slot = 0;
   prefix_rows.tokens = S;
+  // Order on the stream: prep -> prefix attention (tc_ctas CTAs) -> suffix
+  // decode, launched while the prefix grid runs and sized for the other SMs;
+  // it waits for the prefix grid only on its way out -> suffix merge ->
+  // prefix merge -> the two-way merge. Every wait in that chain implies the
+  // completion of the grids before it.
   if (L.tg.enabled) {
     rc = launch_prefill_tc(L.tg, q_g, k_cache, v_cache, prefix_bt, prefix_lens, cu_group,
                            num_members, /*causal=*/0, scale, nullptr, nullptr, &L.tc_shape,
-                           ws + L.tc_ws, st, /*min_q_len=*/1, &prefix_rows, group_members);
+                           ws + L.tc_ws, st, /*min_q_len=*/1, &prefix_rows, group_members,
+                           /*parts=*/1);
     if (rc != PA_OK) return rc;
   }
   // suffix half: slot 1 of every row
   RowsOut suffix_rows = prefix_rows;
   suffix_rows.slot = 1;
   rc = decode_rows(q, k_cache, v_cache, suffix_bt, suffix_cl, scale, &L.suffix_shape,
-                   suffix_rows, ws + L.dec_ws, L.dec_ws_bytes, st);
+                   suffix_rows, ws + L.dec_ws, L.dec_ws_bytes, st, L.tg.enabled ? 1 : 0,
+                   L.suffix_sms);
   if (rc != PA_OK) return rc;
+  if (L.tg.enabled) {
+    rc = launch_prefill_tc(L.tg, q_g, k_cache, v_cache, prefix_bt, prefix_lens, cu_group,
+                           num_members, /*causal=*/0, scale, nullptr, nullptr, &L.tc_shape,
+                           ws + L.tc_ws, st, /*min_q_len=*/1, &prefix_rows, group_members,
+                           /*parts=*/2);
+    if (rc != PA_OK) return rc;
+  }
   return pa_splitk_reduce(part_o, part_lse, S, Hq, 2, kHeadDim, out, lse, stream);
 }

@@ -83,6 +83,11 @@ struct DecodeArgs {
   // instead of out / lse
   RowsOut rows;
   int skip_copy;    // failure-detection hook: flat tile whose copy is left out (-1: none)
+  // 1: the previous grid is not waited for before the work (the grid ahead of
+  // it has already been waited for by every CTA of that previous grid); thread
+  // 0 of each CTA waits for it only on the way out, so that this grid never
+  // completes before it (the cascade's suffix half, beside its prefix half)
+  int late;
 };
 
 // Write 8 dims (one lane's chunk) of one output row as bf16.
@@ -243,7 +248,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const Deco
   // write runs: a warp waits for the write only before it copies the last
   // tile of a (sequence, KV head). Thread 0 of CTA 0 also waits once, so
   // that this grid never completes before the write.
-  if (!a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!a.early && !a.late) asm volatile("griddepcontrol.wait;" ::: "memory");
+  auto late_exit = [&]() {
+    if (a.late && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  };
   PlanInputs in;
   in.context_lens = a.context_lens;
   in.cu_seqlens_q = nullptr;
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const Deco
   in.npairs_cap = S;
   in.num_q_rows = S;
   build_plan(in, P, scratch);  // ends with __syncthreads: barrier inits visible too
-  bool waited = !a.early;
+  bool waited = !a.early || a.late;
   if (a.early && blockIdx.x == 0 && threadIdx.x == 0) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     waited = true;
@@ -325,7 +333,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const Deco
     R0 = P.pair_off[pr] + h * nt + b0;
     R1 = R0 + (b1 - b0);
   }
-  if (R0 >= R1) return;
+  if (R0 >= R1) {
+    late_exit();
+    return;
+  }
 
   const int grp = lane >> 3;   // tokens 4*grp .. 4*grp+3 of a tile
   const int c8 = lane & 7;     // dims 16*c8 .. 16*c8+15
@@ -401,6 +412,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const Deco
       // a copy never landed: give the remaining ones a bounded wait, then stop
       for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
         mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
+      late_exit();
       return;
     }
     unsigned char* st = wbuf + stage * kStageBytes;
@@ -575,6 +587,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const Deco
     if (pidx < R1) issue(stage);
     if (idx + 1 < R1) advance(P, S, Hkv, cp);
   }
+  late_exit();
 }
 
 // Merge the pieces of every (sequence, KV head) that the balanced ranges cut.
@@ -686,8 +699,9 @@ struct DecodeGeometry {
 
 inline size_t plan_smem_bytes(int S) { return sizeof(int) * (4 * (size_t)S + 3 + 40); }
 
+// max_sms > 0: size the balanced grid for that many SMs (the rest are busy).
 template <bool Q8>
-int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
+int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int max_sms = 0) {
   constexpr int NST = Q8 ? kStagesQ8 : kStages;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
@@ -709,7 +723,7 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
         per_sm <= 0)
       return PA_ERR_CUDA;
     g->mode = kBalanced;
-    g->grid = dev.num_sms * per_sm;
+    g->grid = (max_sms > 0 && max_sms < dev.num_sms ? max_sms : dev.num_sms) * per_sm;
     g->workers = g->grid * kWarps;
     g->fixup_smem = plan_smem_bytes(S);
     if (g->fixup_smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
@@ -738,8 +752,10 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g) {
   return PA_OK;
 }
 
-int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool q8 = false) {
-  return q8 ? decode_geometry_t<true>(sh, num_splits, g) : decode_geometry_t<false>(sh, num_splits, g);
+int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool q8 = false,
+                    int max_sms = 0) {
+  return q8 ? decode_geometry_t<true>(sh, num_splits, g, max_sms)
+            : decode_geometry_t<false>(sh, num_splits, g, max_sms);
 }
 
 int check_decode_args(const pa_shape* shape, int num_splits) {
@@ -800,7 +816,8 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
                 const float* k_scale, const float* v_scale, const int32_t* block_tables,
                 const int32_t* context_lens, float scale, pa_bf16* out, float* lse,
                 const pa_shape* shape, int num_splits, void* workspace, size_t workspace_bytes,
-                cudaStream_t st, int early, const RowsOut* rows = nullptr) {
+                cudaStream_t st, int early, const RowsOut* rows = nullptr, int late = 0,
+                int max_sms = 0) {
   const bool q8 = k_scale != nullptr;
   int rc = check_decode_args(shape, num_splits);
   if (rc != PA_OK) return rc;
@@ -814,7 +831,7 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
     return PA_ERR_ARG;
   if (!(scale == scale)) return PA_ERR_ARG;
   DecodeGeometry g;
-  rc = decode_geometry(shape, num_splits, &g, q8);
+  rc = decode_geometry(shape, num_splits, &g, q8, max_sms);
   if (rc != PA_OK) return rc;
   if (g.ws_bytes > 0 &&
       (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256)))
@@ -840,6 +857,8 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   a.num_splits = g.P;
   a.num_workers = g.workers;
   a.early = early;
+  a.late = late;
+  if (late && (early || g.mode != kBalanced)) return PA_ERR_ARG;
   a.skip_copy = g_inject_missing_copy;
   g_inject_missing_copy = -1;
   if (rows) {
@@ -879,9 +898,17 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
 int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
                 const int32_t* block_tables, const int32_t* context_lens, float scale,
                 const pa_shape* shape, const RowsOut& rows, void* workspace,
-                size_t workspace_bytes, cudaStream_t st) {
+                size_t workspace_bytes, cudaStream_t st, int late, int max_sms) {
   return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
-                     nullptr, nullptr, shape, 0, workspace, workspace_bytes, st, 0, &rows);
+                     nullptr, nullptr, shape, 0, workspace, workspace_bytes, st, 0, &rows, late,
+                     max_sms);
+}
+
+size_t decode_rows_workspace_size(const pa_shape* shape, int max_sms) {
+  if (check_decode_args(shape, 0) != PA_OK || shape->num_seqs == 0) return 0;
+  DecodeGeometry g;
+  if (decode_geometry(shape, 0, &g, false, max_sms) != PA_OK) return 0;
+  return g.ws_bytes;
 }
 
 }  // namespace pa

@@ -107,10 +107,12 @@ int launch_cache_write(const pa_bf16* k, const pa_bf16* v, const int64_t* slot_m
                        const pa_shape* shape, cudaStream_t st);
 
 // Balanced decode (pa_decode with num_splits 0) writing fp32 rows (pa_decode.cu).
+// late: see DecodeArgs::late; max_sms > 0 sizes the grid for that many SMs.
 int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
                 const int32_t* block_tables, const int32_t* context_lens, float scale,
                 const pa_shape* shape, const RowsOut& rows, void* workspace,
-                size_t workspace_bytes, cudaStream_t st);
+                size_t workspace_bytes, cudaStream_t st, int late = 0, int max_sms = 0);
+size_t decode_rows_workspace_size(const pa_shape* shape, int max_sms);
 
 // ---------------------------------------------------------------------------
 // tensor maps (pa_varlen.cu)
@@ -133,8 +135,9 @@ struct PrefillTcGeometry {
 };
 
 // min_q_len: sequences with a shorter query window are left to another kernel.
+// max_ctas > 0 caps the grid (one CTA per SM) at that many CTAs.
 int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
-                        PrefillTcGeometry* g, int min_q_len = kTcMinQLen);
+                        PrefillTcGeometry* g, int min_q_len = kTcMinQLen, int max_ctas = 0);
 // rows / row_map (optional): write fp32 rows instead of out / lse, query
 // token i of q landing as token row_map[i] (row_map may be null: identity).
 int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf16* k_cache,
@@ -143,7 +146,8 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
                       int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
                       const pa_shape* sh, void* workspace, cudaStream_t st,
                       int min_q_len = kTcMinQLen, const RowsOut* rows = nullptr,
-                      const int32_t* row_map = nullptr);
+                      const int32_t* row_map = nullptr, int parts = 3);
+// parts: bit 0 launches the attention grid, bit 1 its merge grid.
 
 // Each TU that owns kernels exposes the reader of its device error word.
 unsigned take_error_word_cache(cudaStream_t stream, int* rc);

@@ -792,7 +792,7 @@ size_t plan_bytes(int S, int npairs_cap) {
 }  // namespace
 
 int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
-                        PrefillTcGeometry* g, int min_q_len) {
+                        PrefillTcGeometry* g, int min_q_len, int max_ctas) {
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int G = sh->num_q_heads / sh->num_kv_heads;
@@ -824,7 +824,8 @@ int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
                              (int)g->fixup_smem) != cudaSuccess)
       return PA_ERR_CUDA;
   }
-  g->grid = dev.num_sms;  // one CTA per SM (shared memory and TMEM limit it to one)
+  // one CTA per SM (shared memory and TMEM limit it to one)
+  g->grid = max_ctas > 0 && max_ctas < dev.num_sms ? max_ctas : dev.num_sms;
   g->workers = g->grid;
   g->ws_lse = round_up(sizeof(float) * 2 * kRowsT * (size_t)g->workers, 256);
   g->ws_o = round_up(sizeof(float) * 2 * kRowsT * kHeadDim * (size_t)g->workers, 256);
@@ -837,7 +838,7 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
                       const int32_t* context_lens, const int32_t* cu_seqlens_q,
                       int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
                       const pa_shape* sh, void* workspace, cudaStream_t st, int min_q_len,
-                      const RowsOut* rows, const int32_t* row_map) {
+                      const RowsOut* rows, const int32_t* row_map, int parts) {
   const int G = sh->num_q_heads / sh->num_kv_heads;
   CUtensorMap tmq, tmk, tmv;
   const int64_t pool_rows = sh->num_blocks * sh->num_kv_heads * kBlock;
@@ -868,10 +869,10 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
   char* ws = static_cast<char*>(workspace);
   a.part_lse = reinterpret_cast<float*>(ws);
   a.part_o = reinterpret_cast<float*>(ws + g.ws_lse);
-  if (launch_dependent(paged_prefill_tc_kernel, dim3(g.grid), dim3(kThreadsT), g.smem, st, tmq,
-                       tmk, tmv, a) != cudaSuccess)
+  if ((parts & 1) && launch_dependent(paged_prefill_tc_kernel, dim3(g.grid), dim3(kThreadsT),
+                                      g.smem, st, tmq, tmk, tmv, a) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (launch_dependent(prefill_tc_fixup_kernel, dim3(g.workers, kRowsT / kFixRowsPerCta),
+  if ((parts & 2) && launch_dependent(prefill_tc_fixup_kernel, dim3(g.workers, kRowsT / kFixRowsPerCta),
                        dim3(kFixThreads), g.fixup_smem, st, a) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
