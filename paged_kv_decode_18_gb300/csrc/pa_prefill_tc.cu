@@ -11,23 +11,29 @@
 //
 // A prefill chunk gives each KV head (128/G) x G query rows that share every
 // K/V tile: a real matrix product, so it runs on tcgen05 with accumulators in
-// tensor memory. One CTA per SM, warp-specialised:
-//   warp 0    TMA producer: the tile's 128 query rows (3-D tensor map over q),
-//             then K and V as eight 16-key pool blocks per 128-key tile, found
-//             through the block table (ids fetched one tile ahead);
+// tensor memory. One CTA per SM, warp-specialised (11 warps):
+//   warp 0    TMA producer for the query tiles (3-D tensor map over q; two
+//             buffers, so the next piece's tile lands early) and for K, as
+//             eight 16-key pool blocks per 128-key tile found through the
+//             block table (ids fetched one tile ahead);
+//   warp 10   TMA producer for V; K and V stages have their own full/empty
+//             mbarriers, so a K stage refills as soon as its S is done;
 //   warp 1    allocates 512 TMEM columns and, from one thread, issues the
-//             MMAs: S = Q K^T into one of two S buffers (so the next tile's S
-//             is computed while softmax works on this one), then O += P V into
-//             the O columns; each finished group is signalled by
-//             tcgen05.commit on an mbarrier;
-//   warps 2-5 softmax, one thread per query row (no shuffles): read the S row
-//             from TMEM, mask, exp2, write P (bf16) to shared memory in the
-//             128-byte-swizzled K-major layout the MMA reads; rescale O in TMEM
-//             only when a row maximum grows by more than 2^8 (exact either
-//             way); normalise and write the row at the end of a piece.
+//             MMAs: S = Q K^T into one of two S buffers (the next tile's S is
+//             computed while softmax works on this one), then O_h += P_h V_h
+//             for the two 64-key halves, with P read from tensor memory; each
+//             finished group is signalled by tcgen05.commit on an mbarrier;
+//   warps 2-9 softmax, two threads per query row, one per 64-key half, each
+//             with its own running max, sum and O accumulator: read the S
+//             half from TMEM, mask, exp2, write P (bf16 pairs) back over the S
+//             columns just read; rescale O in TMEM only when a row maximum
+//             grows by more than 2^8 (exact either way); at the end of a piece
+//             the halves exchange (max, sum) through shared memory and write
+//             the normalised row during the next tile.
 // Work is the same equal cut of the batch's flat (query tile, KV head, key
 // tile) list used by the other kernels, at CTA granularity; pieces of a
-// segment cut between CTAs are merged by prefill_tc_fixup_kernel.
+// segment cut between CTAs are merged by prefill_tc_fixup_kernel. Optional
+// fp32 row output with a row map serves the cascade's shared-prefix half.
 #include <cudaTypedefs.h>
 
 #include "pa_device.cuh"
