@@ -217,7 +217,8 @@ __device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)
 }
 
 template <int NWARPS, int NSTAGE, bool Q8>
-__global__ void __launch_bounds__(NWARPS * 32, 2) paged_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
+    paged_decode_kernel(const DecodeArgs a) {
   using L = WarpLayout<NSTAGE, Q8>;
   using F = KvFormat<Q8>;
   constexpr int kStageBytes = F::kStage;
@@ -684,6 +685,11 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part_o,
 // host side
 // ---------------------------------------------------------------------------
 constexpr int kWarps = 6;
+// Batches with no more (sequence, KV head) segments than SMs (long contexts)
+// run 8-warp CTAs, one per SM: each segment spans many warps and a sweep of
+// CTA shapes measured the 8 x 32k batch 10% faster so; the other batches
+// (engine, ragged) run best with 6 warps x 2 CTAs per SM.
+constexpr int kWarpsLong = 8;
 constexpr int kStages = 2;    // bf16: 2 x 8 KB of copies in flight per warp
 constexpr int kStagesQ8 = 3;  // int8: 3 x 4 KB (two CTAs per SM still fit)
 
@@ -695,20 +701,23 @@ struct DecodeGeometry {
   size_t smem = 0;
   size_t fixup_smem = 0;
   size_t ws_desc = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
+  int nwarps = kWarps;  // warps per CTA of the decode grid
 };
 
 inline size_t plan_smem_bytes(int S) { return sizeof(int) * (4 * (size_t)S + 3 + 40); }
 
 // max_sms > 0: size the balanced grid for that many SMs (the rest are busy).
-template <bool Q8>
+template <bool Q8, int NW>
 int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int max_sms = 0) {
   constexpr int NST = Q8 ? kStagesQ8 : kStages;
+  constexpr int kWarps = NW;
+  g->nwarps = NW;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
   g->smem = (size_t)kWarps * WarpLayout<NST, Q8>::kBytes + plan_smem_bytes(S);
   if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
-  auto kern = paged_decode_kernel<kWarps, NST, Q8>;
+  auto kern = paged_decode_kernel<NW, NST, Q8>;
   static std::mutex mu;
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -754,8 +763,13 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int
 
 int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool q8 = false,
                     int max_sms = 0) {
-  return q8 ? decode_geometry_t<true>(sh, num_splits, g, max_sms)
-            : decode_geometry_t<false>(sh, num_splits, g, max_sms);
+  if (q8) return decode_geometry_t<true, kWarps>(sh, num_splits, g, max_sms);
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return PA_ERR_CUDA;
+  const bool long_ctx = num_splits == 0 && max_sms == 0 &&
+                        (int64_t)sh->num_seqs * sh->num_kv_heads <= dev.num_sms;
+  return long_ctx ? decode_geometry_t<false, kWarpsLong>(sh, num_splits, g, max_sms)
+                  : decode_geometry_t<false, kWarps>(sh, num_splits, g, max_sms);
 }
 
 int check_decode_args(const pa_shape* shape, int num_splits) {
@@ -872,8 +886,11 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   const cudaError_t le =
       q8 ? launch_dependent(paged_decode_kernel<kWarps, kStagesQ8, true>, dim3(g.grid),
                             dim3(kWarps * 32), g.smem, st, a)
-         : launch_dependent(paged_decode_kernel<kWarps, kStages, false>, dim3(g.grid),
-                            dim3(kWarps * 32), g.smem, st, a);
+      : g.nwarps == kWarpsLong
+          ? launch_dependent(paged_decode_kernel<kWarpsLong, kStages, false>, dim3(g.grid),
+                             dim3(kWarpsLong * 32), g.smem, st, a)
+          : launch_dependent(paged_decode_kernel<kWarps, kStages, false>, dim3(g.grid),
+                             dim3(kWarps * 32), g.smem, st, a);
   if (le != cudaSuccess) return PA_ERR_CUDA;
   const int wpb = 8;
   if (g.mode == kBalanced) {
