@@ -592,10 +592,12 @@ def run_secondary_varlen(args, dev, B, peak):
 # the oracle on the host cores (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_rate(seed: int, budget_s: float, max_steps: int | None = None):
+def oracle_rate(seed: int, budget_s: float, max_steps: int | None = None,
+                num_threads: int = 0):
     """Time the fp64 oracle on the engine workload: each step is the oracle's
     cache write of the new tokens plus paged attention over a sample of the
-    sequences. Returns (tokens/s, threads, description, steps, seqs/step)."""
+    sequences (num_threads 0 = all host cores). Returns (tokens/s, threads,
+    description, steps, seqs/step)."""
     import numpy as np
 
     from oracle import oracle
@@ -605,13 +607,14 @@ def oracle_rate(seed: int, budget_s: float, max_steps: int | None = None):
     kp = np.full(w.pool_shape(), W.POOL_SENTINEL_BITS, np.uint16)
     vp = kp.copy()
     oracle.reshape_and_cache(w.k_hist, w.v_hist, w.slot_hist, kp, vp, w.block_size)
-    threads = oracle.max_threads()
+    threads = oracle.max_threads() if num_threads <= 0 else num_threads
 
     def one(n_seqs):
         oracle.reshape_and_cache(w.k_new[:n_seqs], w.v_new[:n_seqs], w.slot_new[:n_seqs], kp, vp,
                                  w.block_size)
         oracle.paged_attention(w.q[:n_seqs], kp, vp, w.block_tables[:n_seqs],
-                               w.context_lens[:n_seqs], w.cu_seqlens_q[:n_seqs + 1], w.scale)
+                               w.context_lens[:n_seqs], w.cu_seqlens_q[:n_seqs + 1], w.scale,
+                               num_threads=threads)
 
     t = time.perf_counter()
     one(w.num_seqs)
@@ -783,8 +786,9 @@ def main():
         cpu = None
         if not args.no_cpu_baseline:
             rate, threads, desc, _, _ = oracle_rate(args.seed, 10.0)
+            rate1, _, desc1, _, _ = oracle_rate(args.seed, 3.0, num_threads=1)
             cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                   "sample": desc}
+                   "sample": desc, "value_1_thread": rate1, "sample_1_thread": desc1}
         traffic = traffic_for("engine")
         line = {
             "metric": METRIC,

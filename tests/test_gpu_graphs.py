@@ -98,3 +98,73 @@ def test_varlen_graph_replay():
     torch.cuda.synchronize()
     ref, ref_lse = oracle_attention(w)
     assert_attention_close(out, lse, ref, ref_lse, what="varlen graph")
+
+
+def test_int8_write_and_decode_graph_replay():
+    # quantising cache write + int8 decode captured once; replayed after the
+    # new rows and the queries change in place
+    w = W.engine(seed=63, num_seqs=24, context=300)
+    dev = torch.device("cuda:0")
+    kc, vc, ks, vs = w.empty_pool_i8(dev)
+    B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
+                                kc, vc, ks, vs)
+    k_new, v_new, slots = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
+    q, bt, cl = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    sh = B.shape_of(q, kc, bt)
+    ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
+
+    def step():
+        B.pa_reshape_and_cache_int8(k_new, v_new, slots, kc, vc, ks, vs)
+        B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    gen = torch.Generator().manual_seed(64)
+    k2 = torch.randn(w.k_new.shape, generator=gen).to(torch.bfloat16)
+    v2 = torch.randn(w.v_new.shape, generator=gen).to(torch.bfloat16)
+    q2 = torch.randn(w.q.shape, generator=gen).to(torch.bfloat16)
+    k_new.copy_(k2)
+    v_new.copy_(v2)
+    q.copy_(q2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    w.k_new, w.v_new, w.q = k2, v2, q2
+    from tests.pools import oracle_attention_i8
+    ref, ref_lse = oracle_attention_i8(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="int8 graph replay")
+
+
+def test_cascade_graph_replay():
+    w = W.shared_prompt(seed=65, num_seqs=24, prefix_tokens=512, hi=200)
+    db = DeviceBatch(w)
+    sg, cu, mem, pl, mg, mp = [x.to(db.dev) if torch.is_tensor(x) else x
+                               for x in W.cascade_groups(w)]
+    out = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.dev)
+    sh = B.shape_of(db.q, db.kc, db.block_tables)
+    ws = B.workspace(B.pa_decode_cascade_workspace_size(sh, pl.shape[0], mem.numel(), mg, mp),
+                     db.dev)
+
+    def call():
+        B.pa_decode_cascade(db.q, db.kc, db.vc, db.block_tables, db.context_lens, sg, cu, mem,
+                            pl, mg, mp, w.scale, out, lse, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    q2 = torch.randn(w.q.shape, generator=torch.Generator().manual_seed(66)).to(torch.bfloat16)
+    db.q.copy_(q2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    w.q = q2
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="cascade graph replay")
