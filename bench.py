@@ -323,27 +323,45 @@ def run_ours(args, rank, world, dev):
 
 
 def run_e2e(args, w, dev, B, layers, ws):
-    """Same step through the public calls with host buffers: pinned H2D of the
-    step's inputs, the two library calls, D2H of out and lse, each step."""
+    """Same step through the public calls with host buffers: the step's inputs
+    (q, new K/V, slots, block tables, context lengths) staged in one pinned
+    buffer and copied host-to-device in one copy, the library call, and out +
+    lse (views of one device buffer) copied back in one copy and read on the
+    host, every step."""
     names = ("q", "k_new", "v_new", "slot_new", "block_tables", "context_lens")
-    host = {k: getattr(w, k).pin_memory() for k in names}
-    devb = {k: torch.empty_like(host[k], device=dev) for k in names}
-    out_h = torch.empty(w.q.shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(w.q.shape[:2], dtype=torch.float32).pin_memory()
-    out = torch.empty_like(devb["q"])
-    lse = torch.empty(devb["q"].shape[:2], dtype=torch.float32, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def packed(tensors, device, pinned):
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(off, dtype=torch.uint8, device=device)
+        if pinned:
+            buf = buf.pin_memory()
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for o, t in zip(offs, tensors)]
+        return buf, views
+
+    src = [getattr(w, k).contiguous() for k in names]
+    host_in, host_views = packed(src, "cpu", True)
+    for v, t in zip(host_views, src):
+        v.copy_(t)
+    dev_in, dv = packed(src, dev, False)
+    devb = dict(zip(names, dv))
+    outs = [torch.empty(w.q.shape, dtype=torch.bfloat16),
+            torch.empty(w.q.shape[:2], dtype=torch.float32)]
+    dev_out, (out, lse) = packed(outs, dev, False)
+    host_out, (out_h, lse_h) = packed(outs, "cpu", True)
+    h2d = host_in.numel()
+    d2h = host_out.numel()
     steps = max(1, min(args.steps, 2000))
 
     def step(l):
-        for k in names:
-            devb[k].copy_(host[k], non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         B.pa_append_decode(devb["k_new"], devb["v_new"], devb["slot_new"], devb["q"], l.kc, l.vc,
                            devb["block_tables"], devb["context_lens"], w.scale, out, lse,
                            workspace=ws)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        host_out.copy_(dev_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()  # the result is read on the host
 
     for i in range(max(3, min(args.warmup, 50))):
@@ -356,8 +374,33 @@ def run_e2e(args, w, dev, B, layers, ws):
     e.record()
     torch.cuda.synchronize()
     ms = s.elapsed_time(e)
-    return {"value": w.num_q_tokens * steps / (ms / 1e3), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+    res = {"value": w.num_q_tokens * steps / (ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+    # the same step as an engine runs it: the two copies and the call captured
+    # once in a CUDA graph per layer, replayed and read back every step
+    graphs = []
+    for l in layers:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            dev_in.copy_(host_in, non_blocking=True)
+            B.pa_append_decode(devb["k_new"], devb["v_new"], devb["slot_new"], devb["q"], l.kc,
+                               l.vc, devb["block_tables"], devb["context_lens"], w.scale, out,
+                               lse, workspace=ws)
+            host_out.copy_(dev_out, non_blocking=True)
+        graphs.append(g)
+    for i in range(max(3, min(args.warmup, 50))):
+        graphs[i % LAYERS].replay()
+        torch.cuda.current_stream().synchronize()
+    torch.cuda.synchronize()
+    s.record()
+    for i in range(steps):
+        graphs[i % LAYERS].replay()
+        torch.cuda.current_stream().synchronize()  # the result is read on the host
+    e.record()
+    torch.cuda.synchronize()
+    res["graph_value"] = w.num_q_tokens * steps / (s.elapsed_time(e) / 1e3)
+    return res
 
 
 def run_secondary(args, dev, B):

@@ -717,32 +717,20 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int
   const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
   g->smem = (size_t)kWarps * WarpLayout<NST, Q8>::kBytes + plan_smem_bytes(S);
   if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
-  auto kern = paged_decode_kernel<NW, NST, Q8>;
-  static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)g->smem) != cudaSuccess)
-      return PA_ERR_CUDA;
-  }
+  const void* kern = reinterpret_cast<const void*>(paged_decode_kernel<NW, NST, Q8>);
+  if (!raise_smem_limit(kern)) return PA_ERR_CUDA;
   if (num_splits == 0) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, g->smem) !=
-            cudaSuccess ||
-        per_sm <= 0)
+    if (!kernel_occupancy(kern, kWarps * 32, g->smem, &per_sm) || per_sm <= 0)
       return PA_ERR_CUDA;
     g->mode = kBalanced;
     g->grid = (max_sms > 0 && max_sms < dev.num_sms ? max_sms : dev.num_sms) * per_sm;
     g->workers = g->grid * kWarps;
     g->fixup_smem = plan_smem_bytes(S);
     if (g->fixup_smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      if (g->fixup_smem > 48 * 1024 &&
-          cudaFuncSetAttribute(decode_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)g->fixup_smem) != cudaSuccess)
-        return PA_ERR_CUDA;
-    }
+    if (g->fixup_smem > 48 * 1024 &&
+        !raise_smem_limit(reinterpret_cast<const void*>(decode_fixup_kernel)))
+      return PA_ERR_CUDA;
     g->ws_lse = round_up(sizeof(float) * 2 * kG * (size_t)g->workers, 256);
     g->ws_o = round_up(sizeof(float) * 2 * kG * kHeadDim * (size_t)g->workers, 256);
   } else {

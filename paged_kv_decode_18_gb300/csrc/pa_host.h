@@ -4,6 +4,12 @@
 
 #include <cuda.h>
 #include <nvtx3/nvToolsExt.h>
+
+#include <map>
+#include <mutex>
+#include <set>
+#include <tuple>
+#include <utility>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -40,6 +46,49 @@ inline bool current_device_info(DeviceInfo* out) {
     cache[dev] = d;
   }
   *out = cache[dev];
+  return true;
+}
+
+// A kernel's dynamic shared-memory limit is raised to the device maximum once
+// per (kernel, device); the launches pass their actual size.
+inline bool raise_smem_limit(const void* fn) {
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return false;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({fn, dev.device})) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           dev.max_smem_optin) != cudaSuccess)
+    return false;
+  done.insert({fn, dev.device});
+  return true;
+}
+
+// Resident CTAs per SM of a kernel for a block size and dynamic shared-memory
+// size, queried once per (kernel, device, threads, bytes) and then cached:
+// the host path of a call stays free of driver queries.
+inline bool kernel_occupancy(const void* fn, int threads, size_t smem, int* per_sm) {
+  if (!raise_smem_limit(fn)) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, size_t>, int> cache;
+  const auto key = std::make_tuple(fn, dev, threads, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+      *per_sm = it->second;
+      return true;
+    }
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
+    return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  *per_sm = n;
   return true;
 }
 

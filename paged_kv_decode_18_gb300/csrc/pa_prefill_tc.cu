@@ -819,17 +819,11 @@ int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
   g->fixup_smem = plan_bytes(S, g->npairs_cap);
   if (g->smem > (size_t)dev.max_smem_optin || g->fixup_smem > (size_t)dev.max_smem_optin)
     return PA_ERR_UNSUPPORTED;
-  static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (cudaFuncSetAttribute(paged_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)g->smem) != cudaSuccess)
-      return PA_ERR_CUDA;
-    if (g->fixup_smem > 48 * 1024 &&
-        cudaFuncSetAttribute(prefill_tc_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)g->fixup_smem) != cudaSuccess)
-      return PA_ERR_CUDA;
-  }
+  if (!raise_smem_limit(reinterpret_cast<const void*>(paged_prefill_tc_kernel)))
+    return PA_ERR_CUDA;
+  if (g->fixup_smem > 48 * 1024 &&
+      !raise_smem_limit(reinterpret_cast<const void*>(prefill_tc_fixup_kernel)))
+    return PA_ERR_CUDA;
   // one CTA per SM (shared memory and TMEM limit it to one)
   g->grid = max_ctas > 0 && max_ctas < dev.num_sms ? max_ctas : dev.num_sms;
   g->workers = g->grid;

@@ -498,19 +498,9 @@ int varlen_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
   const size_t plan = sizeof(int) * ((size_t)g->npairs_cap + 1 + 3 * (size_t)S + 2 + 40);
   g->smem = 1024 + (size_t)kWarps * kStages * kStageBytes + (size_t)kWarps * kStages * 8 + plan;
   if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
-  auto kern = paged_varlen_kernel<kWarps, kStages>;
-  static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g->smem) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
-  }
+  const void* kern = reinterpret_cast<const void*>(paged_varlen_kernel<kWarps, kStages>);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, g->smem) !=
-          cudaSuccess ||
-      per_sm <= 0)
-    return PA_ERR_CUDA;
+  if (!kernel_occupancy(kern, kWarps * 32, g->smem, &per_sm) || per_sm <= 0) return PA_ERR_CUDA;
   g->grid = dev.num_sms * per_sm;
   g->workers = g->grid * kWarps;
   g->ws_desc = round_up(sizeof(int) * kDescInts * (size_t)g->workers, 256);
