@@ -421,56 +421,83 @@ __global__ void __launch_bounds__(NWARPS * 32)
 }
 
 // Merge the pieces of (sequence, query tile, KV head) segments cut by the
-// balanced ranges; one warp per worker boundary, rows looped.
-__global__ void varlen_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
-                                    const float* __restrict__ part_lse,
-                                    const int32_t* __restrict__ cu_seqlens_q, int num_workers,
-                                    int Hq, int G, int QT, uint16_t* __restrict__ out,
-                                    float* __restrict__ lse) {
+// balanced ranges. One CTA per worker boundary; a warp merges four rows at
+// once (eight lanes per row, sixteen dims per lane), online over the pieces,
+// four pieces at a time with all their loads in flight. Partials are read
+// through L2 (ld.global.cg): other SMs wrote them.
+constexpr int kFixWarps = kRows / 4;
+
+__global__ void __launch_bounds__(kFixWarps * 32)
+    varlen_fixup_kernel(const int* __restrict__ desc, const float* __restrict__ part_o,
+                        const float* __restrict__ part_lse,
+                        const int32_t* __restrict__ cu_seqlens_q, int num_workers, int Hq, int G,
+                        int QT, uint16_t* __restrict__ out, float* __restrict__ lse) {
   // the next grid in the stream may start its own preparation now; it waits
   // for this grid before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x;
   if (w >= num_workers) return;
   const int* d = desc + (size_t)w * kDescInts;
-  const int s = d[0];
+  const int s = __ldcg(d);
   if (s < 0) return;
-  const int qt = d[1], h = d[2], last = d[3], slot_prev = d[4];
+  const int qt = __ldcg(d + 1), h = __ldcg(d + 2), last = __ldcg(d + 3),
+            slot_prev = __ldcg(d + 4);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = warp * 4 + (lane >> 3);
+  const int d0 = (lane & 7) * 16;
   const int q0 = cu_seqlens_q[s], lq = cu_seqlens_q[s + 1] - q0;
-  for (int r = 0; r < kRows; ++r) {
-    const int tok = qt * QT + r / G;
-    if (tok >= lq) continue;
-    float mx = neg_inf();
-    for (int x = w - 1; x <= last; ++x) {
-      const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
-      mx = fmaxf(mx, part_lse[slot * kRows + r]);
+  const int tok = qt * QT + r / G;
+  if (tok >= lq) return;
+  const int npieces = last - w + 2;  // workers w-1 .. last
+  float m = neg_inf(), sum = 0.f;
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  for (int i0 = 0; i0 < npieces; i0 += 4) {
+    float li[4];
+    float4 x[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      li[u] = neg_inf();
+      x[u][0] = x[u][1] = x[u][2] = x[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i0 + u < npieces) {
+        const size_t sl = (size_t)(w - 1 + i0 + u) * 2 + (i0 + u == 0 ? slot_prev : 0);
+        li[u] = __ldcg(part_lse + sl * kRows + r);
+        const float4* src = reinterpret_cast<const float4*>(part_o + (sl * kRows + r) * kHeadDim + d0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[u][k] = __ldcg(src + k);
+      }
     }
-    float sum = 0.f;
-    for (int x = w - 1; x <= last; ++x) {
-      const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
-      sum += ex2((part_lse[slot * kRows + r] - mx) * kLog2e);
+    const float mn = fmaxf(fmaxf(m, fmaxf(li[0], li[1])), fmaxf(li[2], li[3]));
+    if (mn == neg_inf()) continue;
+    const float shrink = m == neg_inf() ? 0.f : ex2((m - mn) * kLog2e);
+    sum *= shrink;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] *= shrink;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float wt = li[u] == neg_inf() ? 0.f : ex2((li[u] - mn) * kLog2e);
+      sum += wt;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[4 * k + 0] = fmaf(wt, x[u][k].x, acc[4 * k + 0]);
+        acc[4 * k + 1] = fmaf(wt, x[u][k].y, acc[4 * k + 1]);
+        acc[4 * k + 2] = fmaf(wt, x[u][k].z, acc[4 * k + 2]);
+        acc[4 * k + 3] = fmaf(wt, x[u][k].w, acc[4 * k + 3]);
+      }
     }
-    const float LSE = mx + lg2(sum) * kLn2;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int x = w - 1; x <= last; ++x) {
-      const size_t slot = (size_t)x * 2 + (x == w - 1 ? slot_prev : 0);
-      const float wt = ex2((part_lse[slot * kRows + r] - LSE) * kLog2e);
-      const float4 v =
-          *reinterpret_cast<const float4*>(part_o + (slot * kRows + r) * kHeadDim + lane * 4);
-      acc.x = fmaf(wt, v.x, acc.x);
-      acc.y = fmaf(wt, v.y, acc.y);
-      acc.z = fmaf(wt, v.z, acc.z);
-      acc.w = fmaf(wt, v.w, acc.w);
-    }
-    const int64_t orow = ((int64_t)q0 + tok) * Hq + (int64_t)h * G + r % G;
-    uint2 ov;
-    ov.x = cvt_bf16x2(acc.x, acc.y);
-    ov.y = cvt_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(out + orow * kHeadDim + lane * 4) = ov;
-    if (lse && lane == 0) lse[orow] = LSE;
+    m = mn;
   }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const float LSE = sum > 0.f ? m + lg2(sum) * kLn2 : neg_inf();
+  const int64_t orow = ((int64_t)q0 + tok) * Hq + (int64_t)h * G + r % G;
+  uint4* dst = reinterpret_cast<uint4*>(out + orow * kHeadDim + d0);
+  dst[0] = make_uint4(cvt_bf16x2(acc[0] * inv, acc[1] * inv), cvt_bf16x2(acc[2] * inv, acc[3] * inv),
+                      cvt_bf16x2(acc[4] * inv, acc[5] * inv), cvt_bf16x2(acc[6] * inv, acc[7] * inv));
+  dst[1] = make_uint4(cvt_bf16x2(acc[8] * inv, acc[9] * inv), cvt_bf16x2(acc[10] * inv, acc[11] * inv),
+                      cvt_bf16x2(acc[12] * inv, acc[13] * inv), cvt_bf16x2(acc[14] * inv, acc[15] * inv));
+  if (lse && (lane & 7) == 0) lse[orow] = LSE;
 }
 
 // ---------------------------------------------------------------------------
@@ -640,9 +667,8 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   if (launch_dependent(paged_varlen_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
                        g.smem, st, tmk, tmv, a) != cudaSuccess)
     return PA_ERR_CUDA;
-  const int wpb = 8;
-  if (launch_dependent(varlen_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32), 0,
-                       st, (const int*)a.desc, (const float*)a.part_o, (const float*)a.part_lse,
+  if (launch_dependent(varlen_fixup_kernel, dim3(g.workers), dim3(kFixWarps * 32), 0, st,
+                       (const int*)a.desc, (const float*)a.part_o, (const float*)a.part_lse,
                        cu_seqlens_q, g.workers, a.Hq, a.G, a.QT, (uint16_t*)out,
                        lse) != cudaSuccess)
     return PA_ERR_CUDA;
