@@ -107,7 +107,11 @@ __device__ __forceinline__ void store_f8(float* dst, const float (&v)[8], float 
 
 // Merge the pieces of one cut (sequence, KV head) segment -- the a7 formula
 // over workers w-1 .. job.last -- and write its two output rows. One warp.
-// Partials are read through L2 (ld.global.cg): other SMs wrote them.
+// Partials are read through L2 (ld.global.cg): other SMs wrote them. The
+// log-sum-exps and vectors of up to eight pieces are loaded together, so a
+// typical cut costs one round trip to L2.
+constexpr int kMergeChunk = 8;
+
 __device__ __forceinline__ void merge_segment(const MergeJob& job, int w, int lane,
                                               const float* __restrict__ part_o,
                                               const float* __restrict__ part_lse, int Hq,
@@ -115,49 +119,59 @@ __device__ __forceinline__ void merge_segment(const MergeJob& job, int w, int la
                                               float* __restrict__ lse, const RowsOut& rows) {
   const int s = job.s, h = job.h, last = job.last, slot_prev = job.slot_prev;
   const int npieces = last - w + 2;  // workers w-1 .. last
+  auto slot_of = [&](int i) -> size_t {
+    return (size_t)(w - 1 + i) * 2 + (i == 0 ? slot_prev : 0);
+  };
   float4 acc[kG];
   for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // each round handles 32 pieces: lane i holds piece i's lse values while the
-  // partial vectors of the round are loaded at the same time
+  // each round handles kMergeChunk pieces: lane i holds piece i's lse values
   float mx[kG] = {neg_inf(), neg_inf()}, sum[kG] = {0.f, 0.f};
-  for (int i0 = 0; i0 < npieces; i0 += 32) {
-    const int n = min(32, npieces - i0);
+  for (int i0 = 0; i0 < npieces; i0 += kMergeChunk) {
+    const int n = min(kMergeChunk, npieces - i0);
     float li[kG] = {neg_inf(), neg_inf()};
     if (lane < n) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(part_lse + ((size_t)(w - 1 + i0 + lane) * 2 + (i0 + lane == 0 ? slot_prev : 0)) * kG));
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(part_lse + slot_of(i0 + lane) * kG));
       li[0] = v.x;
       li[1] = v.y;
     }
-    float m[kG], e[kG];
+    float4 o[kMergeChunk][kG];
+#pragma unroll
+    for (int j = 0; j < kMergeChunk; ++j) {
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        o[j][g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < n)
+          o[j][g] = __ldcg(reinterpret_cast<const float4*>(
+              part_o + (slot_of(i0 + j) * kG + g) * kHeadDim + lane * 4));
+      }
+    }
+    float e[kG];
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
-      m[g] = li[g];
+      float m = li[g];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m[g] = fmaxf(m[g], __shfl_xor_sync(kFull, m[g], o));
-      m[g] = fmaxf(m[g], mx[g]);
+      for (int x = 16; x > 0; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
+      m = fmaxf(m, mx[g]);
       // rescale what earlier rounds accumulated to the new maximum
-      const float r = ex2((mx[g] - m[g]) * kLog2e);
+      const float r = ex2((mx[g] - m) * kLog2e);
       sum[g] *= r;
       acc[g].x *= r; acc[g].y *= r; acc[g].z *= r; acc[g].w *= r;
-      e[g] = ex2((li[g] - m[g]) * kLog2e);  // unnormalised weight of piece lane
+      e[g] = ex2((li[g] - m) * kLog2e);  // unnormalised weight of piece lane
       float t = e[g];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+      for (int x = 16; x > 0; x >>= 1) t += __shfl_xor_sync(kFull, t, x);
       sum[g] += t;
-      mx[g] = m[g];
+      mx[g] = m;
     }
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
-      const size_t slot = (size_t)(w - 1 + i0 + j) * 2 + (i0 + j == 0 ? slot_prev : 0);
+#pragma unroll
+    for (int j = 0; j < kMergeChunk; ++j) {
 #pragma unroll
       for (int g = 0; g < kG; ++g) {
         const float wt = __shfl_sync(kFull, e[g], j);
-        const float4 o =
-            __ldcg(reinterpret_cast<const float4*>(part_o + (slot * kG + g) * kHeadDim + lane * 4));
-        acc[g].x = fmaf(wt, o.x, acc[g].x);
-        acc[g].y = fmaf(wt, o.y, acc[g].y);
-        acc[g].z = fmaf(wt, o.z, acc[g].z);
-        acc[g].w = fmaf(wt, o.w, acc[g].w);
+        acc[g].x = fmaf(wt, o[j][g].x, acc[g].x);
+        acc[g].y = fmaf(wt, o[j][g].y, acc[g].y);
+        acc[g].z = fmaf(wt, o[j][g].z, acc[g].z);
+        acc[g].w = fmaf(wt, o[j][g].w, acc[g].w);
       }
     }
   }
