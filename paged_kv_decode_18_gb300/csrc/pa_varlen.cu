@@ -58,6 +58,12 @@ struct VarlenArgs {
   float* part_o;    // [NW*2][16][D]
   float* part_lse;  // [NW*2][16]
   int* desc;        // [NW][kDescInts]
+  // 1: the grid ahead (the tcgen05 prefill grid of the same call, which
+  // waited for its own predecessor before letting this grid launch) is not
+  // waited for before the work: this grid reads nothing it writes and writes
+  // nothing it reads, so verify tiles stream on the SMs that the prefill
+  // grid's tail leaves free
+  int late;
 };
 
 // byte offset of (row, 16-byte chunk) inside a 16 x 128 B box written by TMA
@@ -73,9 +79,8 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 }
 
 template <int NWARPS, int NSTAGE>
-__global__ void __launch_bounds__(NWARPS * 32)
-    paged_varlen_kernel(const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const VarlenArgs a) {
+__device__ __forceinline__ void varlen_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                            const VarlenArgs& a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // stage buffers need 1024-byte alignment for the swizzle pattern
   const uint32_t raw = smem_addr(smem_raw);
@@ -103,8 +108,8 @@ __global__ void __launch_bounds__(NWARPS * 32)
     prefetch_tensormap(&tmv);
   }
   // launched as a programmatic dependent of the previous grid: wait for it
-  // before reading anything it may have written
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // before reading anything it may have written (late: see VarlenArgs)
+  if (!a.late) asm volatile("griddepcontrol.wait;" ::: "memory");
   PlanInputs in;
   in.context_lens = a.context_lens;
   in.cu_seqlens_q = a.cu_seqlens_q;
@@ -420,6 +425,16 @@ __global__ void __launch_bounds__(NWARPS * 32)
   }
 }
 
+template <int NWARPS, int NSTAGE>
+__global__ void __launch_bounds__(NWARPS * 32)
+    paged_varlen_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const VarlenArgs a) {
+  varlen_body<NWARPS, NSTAGE>(tmk, tmv, a);
+  // late: thread 0 of each CTA waits for the grid ahead on the way out, so
+  // this grid never completes before it
+  if (a.late && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Merge the pieces of (sequence, query tile, KV head) segments cut by the
 // balanced ranges. One CTA per worker boundary; a warp merges four rows at
 // once (eight lanes per row, sixteen dims per lane), online over the pieces,
@@ -658,15 +673,31 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   a.part_o = reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Sequences with long query chunks (prefill) run as tcgen05 tiles of 128
+  // rows, the others (verify) on the mma.sync kernel; the prefill grid goes
+  // first. When the batch surely holds short sequences (fewer than
+  // kTcMinQLen query tokens per sequence on average), the verify grid follows
+  // it as a late dependent, so verify CTAs start on each SM that the prefill
+  // grid's tail frees, and the prefill merge moves behind the verify grid.
+  // Otherwise (prefill-only batches) the prefill merge follows its own grid
+  // directly, one grid-completion hop earlier.
+  const bool overlap = tg.enabled && num_q_tokens < (int64_t)kTcMinQLen * shape->num_seqs;
+  a.late = overlap ? 1 : 0;
   if (tg.enabled) {
-    // sequences with long query chunks (prefill): tcgen05 tiles of 128 rows
     rc = launch_prefill_tc(tg, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
-                           num_q_tokens, causal, scale, out, lse, shape, ws + g.ws_bytes, st);
+                           num_q_tokens, causal, scale, out, lse, shape, ws + g.ws_bytes, st,
+                           kTcMinQLen, nullptr, nullptr, /*parts=*/overlap ? 1 : 3);
     if (rc != PA_OK) return rc;
   }
   if (launch_dependent(paged_varlen_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
                        g.smem, st, tmk, tmv, a) != cudaSuccess)
     return PA_ERR_CUDA;
+  if (overlap) {
+    rc = launch_prefill_tc(tg, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
+                           num_q_tokens, causal, scale, out, lse, shape, ws + g.ws_bytes, st,
+                           kTcMinQLen, nullptr, nullptr, /*parts=*/2);
+    if (rc != PA_OK) return rc;
+  }
   if (launch_dependent(varlen_fixup_kernel, dim3(g.workers), dim3(kFixWarps * 32), 0, st,
                        (const int*)a.desc, (const float*)a.part_o, (const float*)a.part_lse,
                        cu_seqlens_q, g.workers, a.Hq, a.G, a.QT, (uint16_t*)out,
