@@ -131,12 +131,15 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == B.PA_ERR_WORKSPACE
 
 
-@pytest.mark.parametrize("case", ["tiny", "engine", "ragged_small"])
+APPEND_CASES = dict(CASES, ragged_600=("ragged", dict(num_seqs=600, max_context=300)))
+
+
+@pytest.mark.parametrize("case", ["tiny", "engine", "ragged_small", "ragged_600"])
 def test_append_decode_equals_two_calls(case):
     """pa_append_decode (write + decode in one call, the decode's preparation
     overlapping the write) gives the same pool bytes as pa_reshape_and_cache
-    and the same results as pa_decode."""
-    name, sizes = CASES[case]
+    and the same results as pa_decode, from a handful of new rows to 600."""
+    name, sizes = APPEND_CASES[case]
     w = W.make(name, seed=20, **sizes)
     ref = DeviceBatch(w)                  # history + new tokens written
     ref_out, ref_lse = ref.decode(0)
@@ -157,3 +160,36 @@ def test_append_decode_equals_two_calls(case):
         assert torch.equal(lse, ref_lse)
     ro, rl = oracle_attention(w)
     assert_attention_close(out, lse, ro, rl, what=f"append/{case}")
+
+
+def test_append_decode_any_token_order_skips_and_bad_slots():
+    """New rows in any token order, with a skipped token (slot < 0) and an
+    out-of-range slot mixed in: the same pool bytes and results as the two
+    calls, and the bad slot flagged as pa_reshape_and_cache flags it."""
+    name, sizes = CASES["ragged_small"]
+    w = W.make(name, seed=22, **sizes)
+    ref = DeviceBatch(w)
+    ref_out, ref_lse = ref.decode(0)
+    fused = DeviceBatch(w, write_new=False)
+    n = fused.k_new.shape[0]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(5)).to(fused.dev)
+    g = torch.Generator().manual_seed(6)
+    extra = torch.randn((2,) + tuple(fused.k_new.shape[1:]), generator=g).to(torch.bfloat16)
+    extra = extra.to(fused.dev)
+    bad = torch.tensor([-1, fused.kc.shape[0] * fused.kc.shape[2] + 5], dtype=torch.int64,
+                       device=fused.dev)
+    k_new = torch.cat([fused.k_new[perm], extra])
+    v_new = torch.cat([fused.v_new[perm], -extra])
+    slots = torch.cat([fused.slot_new[perm], bad])
+    out = torch.empty_like(fused.q)
+    lse = torch.empty(fused.q.shape[:2], dtype=torch.float32, device=fused.dev)
+    sh = B.shape_of(fused.q, fused.kc, fused.block_tables)
+    ws = B.workspace(B.pa_decode_workspace_size(sh, 0), fused.dev)
+    B.pa_append_decode(k_new, v_new, slots, fused.q, fused.kc, fused.vc, fused.block_tables,
+                       fused.context_lens, w.scale, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == B.PA_DEVERR_SLOT_RANGE
+    assert torch.equal(fused.kc.view(torch.int16), ref.kc.view(torch.int16))
+    assert torch.equal(fused.vc.view(torch.int16), ref.vc.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse, ref_lse)
