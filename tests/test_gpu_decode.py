@@ -193,3 +193,46 @@ def test_append_decode_any_token_order_skips_and_bad_slots():
     assert torch.equal(fused.vc.view(torch.int16), ref.vc.view(torch.int16))
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("variant", ["permuted", "skipped", "bad_slot"])
+def test_append_decode_one_row_per_sequence_mappings(variant):
+    """One new token per sequence, as a decode step has, under mappings other
+    than token t -> its own sequence's last position: tokens permuted, a
+    skipped token (slot < 0), an out-of-range slot. Pool bytes, results and
+    error bits equal those of pa_reshape_and_cache followed by pa_decode."""
+    name, sizes = CASES["ragged_small"]
+    w = W.make(name, seed=23, **sizes)
+    dev_batch = DeviceBatch(w, write_new=False)
+    k_new, v_new, slots = dev_batch.k_new, dev_batch.v_new, dev_batch.slot_new.clone()
+    if variant == "permuted":
+        perm = torch.randperm(k_new.shape[0], generator=torch.Generator().manual_seed(7))
+        perm = perm.to(dev_batch.dev)
+        k_new, v_new, slots = k_new[perm], v_new[perm], slots[perm]
+    elif variant == "skipped":
+        slots[3] = -1
+    else:
+        slots[5] = dev_batch.kc.shape[0] * dev_batch.kc.shape[2] + 7
+    expect_err = B.PA_DEVERR_SLOT_RANGE if variant == "bad_slot" else 0
+
+    ref = DeviceBatch(w, write_new=False)
+    B.pa_reshape_and_cache(k_new, v_new, slots, ref.kc, ref.vc)
+    ref_out, ref_lse = ref.decode(0)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == expect_err
+
+    fused = dev_batch
+    out = torch.empty_like(fused.q)
+    lse = torch.empty(fused.q.shape[:2], dtype=torch.float32, device=fused.dev)
+    sh = B.shape_of(fused.q, fused.kc, fused.block_tables)
+    ws = B.workspace(B.pa_decode_workspace_size(sh, 0), fused.dev)
+    B.pa_append_decode(k_new, v_new, slots, fused.q, fused.kc, fused.vc, fused.block_tables,
+                       fused.context_lens, w.scale, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == expect_err
+    assert torch.equal(fused.kc.view(torch.int16), ref.kc.view(torch.int16))
+    assert torch.equal(fused.vc.view(torch.int16), ref.vc.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    # bit patterns: a skipped token leaves the pool's sentinel (NaN) row in
+    # place, read the same way by both paths
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
