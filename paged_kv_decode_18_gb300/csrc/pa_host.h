@@ -15,8 +15,6 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "pa.h"
 
 namespace pa {
