@@ -41,7 +41,7 @@ UNIT = "tokens/s"
 WORKLOAD = ("engine-shaped decode: batch 64, q_len 1, every context 384, 16 Q / 8 KV heads, "
             "head_dim 128, block 16, bf16, shuffled pool; step = cache write of 64 new "
             "tokens + paged decode attention")
-LAYERS = 4                      # rotated KV caches (4 x 100.7 MB > L2)
+LAYERS = 28                     # one KV cache per layer of the Qwen3-0.6B shape (28 x 100.7 MB)
 FALLBACK_HBM_GBS = 6800.0       # only if MEASURED_PEAKS.json is missing
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
@@ -234,8 +234,9 @@ def run_ours(args, rank, world, dev):
                     w.scale, out, lse, num_splits=0, workspace=ws)
 
     # CUDA graphs, as an engine captures its decode step: one graph runs the
-    # step of all LAYERS layers back to back (graph launch cost is paid once
-    # per replay, not per layer); single-layer graphs cover a remainder.
+    # attention step of every layer of the model back to back, each layer on
+    # its own KV cache (graph launch cost is paid once per replay, not per
+    # layer); single-layer graphs cover a remainder.
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -525,7 +526,7 @@ def run_secondary_cascade(args, dev, B, peak):
 
 def run_secondary_int8(args, dev, B, peak):
     """Decode over the INT8 pool (quantised cache write, fused dequant): the
-    engine batch rotated over 4 layer pools, the ragged and the long batch."""
+    engine batch rotated over the layer pools, the ragged and the long batch."""
     from paged_kv_decode_18_gb300 import workloads as W
 
     res = {}
