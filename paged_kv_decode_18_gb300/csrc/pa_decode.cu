@@ -28,6 +28,11 @@
 // A batch is cut into equal tile ranges over all resident warps (num_splits
 // 0), so ragged batches and long contexts balance; a (sequence, KV head) cut
 // by a range boundary leaves partials that a small merge kernel combines.
+// The same kernel, templated on the pool format, serves the INT8 pool (one
+// fp32 scale per (token, KV head) row): the K dot products run on the int8
+// codes with dp4a against q as 16-bit fixed point in two byte limbs, the V
+// codes become fp32 exactly before their products, and the row scales fold
+// into the dot product and the softmax weight.
 #include "pa_device.cuh"
 #include "pa_host.h"
 
