@@ -29,10 +29,10 @@
 // 0), so ragged batches and long contexts balance; a (sequence, KV head) cut
 // by a range boundary leaves partials that a small merge kernel combines.
 // The same kernel, templated on the pool format, serves the INT8 pool (one
-// fp32 scale per (token, KV head) row): the K dot products run on the int8
-// codes with dp4a against q as 16-bit fixed point in two byte limbs, the V
-// codes become fp32 exactly before their products, and the row scales fold
-// into the dot product and the softmax weight.
+// fp32 scale per (token, KV head) row): the codes become fp32 exactly (a byte
+// permute into the mantissa of 2^23 and one packed subtraction) before the
+// same products, and the row scales fold into the dot product and the softmax
+// weight.
 #include "pa_device.cuh"
 #include "pa_host.h"
 
@@ -218,42 +218,6 @@ __device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& lo, float2& hi) {
 }
 
 // The 16 dims 16*c8 .. 16*c8+15 of one token row in stage memory, as 8 pairs.
-// q (already times scale * log2 e) as 16-bit fixed point for dot products
-// with int8 codes: step = max |q| / 32639 over the warp (both heads), value
-// v = rint(q / step) in [-32639, 32639], split into signed bytes hi = (v + 128)
-// >> 8 and lo = v - 256 hi (both in [-128, 127]); four dims per word, dims
-// 16*c8 + 4j .. +3 in word j. Rounding q to the step is an error of at most
-// 1/65278 of the largest |q| per element. Returns the step (0 for q = 0).
-__device__ __forceinline__ float q_limbs_i8(const float2 (&q2)[kG][8], int (&hi)[kG][4],
-                                            int (&lo)[kG][4]) {
-  float mx = 0.f;
-#pragma unroll
-  for (int g = 0; g < kG; ++g)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fmaxf(fabsf(q2[g][j].x), fabsf(q2[g][j].y)));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  const float inv = mx > 0.f ? 32639.f / mx : 0.f;
-#pragma unroll
-  for (int g = 0; g < kG; ++g) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float x[4] = {q2[g][2 * j].x, q2[g][2 * j].y, q2[g][2 * j + 1].x, q2[g][2 * j + 1].y};
-      uint32_t h = 0u, l = 0u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int v = min(32639, max(-32639, __float2int_rn(x[e] * inv)));
-        const int vh = (v + 128) >> 8;
-        h |= (uint32_t)(vh & 0xff) << (8 * e);
-        l |= (uint32_t)((v - 256 * vh) & 0xff) << (8 * e);
-      }
-      hi[g][j] = (int)h;
-      lo[g][j] = (int)l;
-    }
-  }
-  return mx / 32639.f;
-}
-
 template <bool Q8>
 __device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)[8]) {
   if constexpr (Q8) {
@@ -455,12 +419,6 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
   // both query heads; fp32 pairs go through the packed (f32x2) FMA pipe.
   TilePos cp = locate(P, S, Hkv, R0);
   float2 q2[kG][8];    // scaled q, dims (16*c8 + 2j, +1)
-  // int8 pool: q * scale * log2(e) as 16-bit fixed point in steps of q_step,
-  // split into two signed byte limbs (value = 256 * hi + lo), four dims per
-  // word (dims 16*c8 + 4j .. +3), so the K dot products run on the int8
-  // codes as they are (dp4a) -- see q_limbs_i8
-  int q_hi[kG][4], q_lo[kG][4];
-  float q_step = 0.f;
   float2 acc[kG][8];   // output accumulator, same dims
   float m0 = neg_inf(), m1 = neg_inf(), l_lane = 0.f;
   int piece_b0 = 0;
@@ -491,7 +449,6 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
           acc[g][j] = make_float2(0.f, 0.f);
         }
       }
-      if constexpr (Q8) q_step = q_limbs_i8(q2, q_hi, q_lo);
       m0 = neg_inf();
       m1 = neg_inf();
       l_lane = 0.f;
@@ -505,33 +462,16 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
     const unsigned char* Ks = st + grp * 4 * F::kRow + c8 * (F::kRow / 8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      if constexpr (Q8) {
-        // 16 codes of the token row against the fixed-point q limbs: exact
-        // integer dot products (|256 hi + lo| < 2^31), in q_step units
-        const uint4 w = *reinterpret_cast<const uint4*>(Ks + i * F::kRow);
-        const int wk[4] = {(int)w.x, (int)w.y, (int)w.z, (int)w.w};
+      float2 kf[8];
+      load_row16<Q8>(Ks + i * F::kRow, kf);
+      float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < kG; ++g) {
-          int hi = 0, lo = 0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            hi = __dp4a(wk[j], q_hi[g][j], hi);
-            lo = __dp4a(wk[j], q_lo[g][j], lo);
-          }
-          sc[2 * i + g] = (float)(hi * 256 + lo);
-        }
-      } else {
-        float2 kf[8];
-        load_row16<Q8>(Ks + i * F::kRow, kf);
-        float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          d0 = __ffma2_rn(q2[0][j], kf[j], d0);
-          d1 = __ffma2_rn(q2[1][j], kf[j], d1);
-        }
-        sc[2 * i] = d0.x + d0.y;
-        sc[2 * i + 1] = d1.x + d1.y;
+      for (int j = 0; j < 8; ++j) {
+        d0 = __ffma2_rn(q2[0][j], kf[j], d0);
+        d1 = __ffma2_rn(q2[1][j], kf[j], d1);
       }
+      sc[2 * i] = d0.x + d0.y;
+      sc[2 * i + 1] = d1.x + d1.y;
     }
     // reduce-scatter over the 8 lanes of this group: value v = 2*i + g ends in
     // the lane with (lane & 7) == v
@@ -547,9 +487,9 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
       }
     }
     const int tok = grp * 4 + ((lane & 7) >> 1);
-    // int8: the q step and the row's K scale multiply its dot product
+    // int8: the row's K scale multiplies its dot product
     float s_val = sc[0];
-    if constexpr (Q8) s_val *= q_step * reinterpret_cast<const float*>(st + F::kScaleOff)[tok];
+    if constexpr (Q8) s_val *= reinterpret_cast<const float*>(st + F::kScaleOff)[tok];
     s_val = tok < nvalid ? s_val : neg_inf();
 
     // ---- online softmax (log2 domain) ------------------------------------------
