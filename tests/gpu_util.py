@@ -69,6 +69,38 @@ class DeviceBatch:
         return out, lse
 
 
+class Int8Batch:
+    """A workload on the GPU with its int8 pool written by the CUDA quantising
+    cache write (history first, then the step's new tokens)."""
+
+    def __init__(self, w):
+        dev = device()
+        self.w, self.dev = w, dev
+        self.kc, self.vc, self.ks, self.vs = w.empty_pool_i8(dev)
+        if w.k_hist.shape[0]:
+            B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
+                                        self.kc, self.vc, self.ks, self.vs)
+        B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev),
+                                    self.kc, self.vc, self.ks, self.vs)
+        self.q = w.q.to(dev)
+        self.bt = w.block_tables.to(dev)
+        self.cl = w.context_lens.to(dev)
+
+    def pools(self):
+        return (self.kc.cpu().numpy(), self.vc.cpu().numpy(), self.ks.cpu().numpy(),
+                self.vs.cpu().numpy())
+
+    def decode(self, num_splits=0, with_lse=True):
+        out = torch.empty_like(self.q)
+        lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=self.dev) \
+            if with_lse else None
+        sh = B.shape_of(self.q, self.kc, self.bt)
+        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, num_splits), self.dev)
+        B.pa_decode_int8(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.cl,
+                         self.w.scale, out, lse, num_splits=num_splits, workspace=ws)
+        return out, lse
+
+
 def assert_attention_close(out, lse, ref_out, ref_lse, rows=None, what=""):
     """|gpu - ref| <= 1e-2 + 1e-2 |ref| for out (bf16 vs fp64), |dlse| <= 1e-3."""
     got = out.float().cpu().numpy().astype(np.float64)

@@ -280,3 +280,66 @@ def test_paged_attention_rejects_bad_block_id():
     bt[0, 0] = w.num_blocks
     with pytest.raises(oracle.OracleError):
         oracle.paged_attention(w.q, kp, vp, bt, w.context_lens, w.cu_seqlens_q, w.scale)
+
+
+# --------------------------------------------------------------------------
+# non-causal windows longer than their context
+# --------------------------------------------------------------------------
+
+def _queries_over_pool(w, q_lens, seed):
+    """A fresh set of query rows (q_lens[s] per sequence) over w's pool:
+    (q [Tq, Hq, D] bf16, cu_seqlens_q [S + 1] int32)."""
+    g = torch.Generator().manual_seed(seed)
+    tq = int(sum(q_lens))
+    q = torch.randn(tq, w.num_q_heads, w.head_dim, generator=g).to(torch.bfloat16)
+    cu = torch.zeros(len(q_lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int32), 0)
+    return q, cu
+
+
+def test_non_causal_window_longer_than_context_matches_sdpa():
+    # S20 "The conflicts" / prefix caching: several sequences' queries attend
+    # one shared context at once, so a non-causal window may hold more query
+    # rows than the context has keys. Every row then sees the whole context:
+    # torch SDPA in float64 with no mask, GQA expanded, is the reference.
+    w = W.build("nc", 21, [3, 9, 20, 16], [1, 1, 1, 1], pool_factor=1.5, causal=False,
+                num_q_heads=4, num_kv_heads=2, head_dim=8, block_size=4, scale=0.41)
+    kp, vp = oracle_pools(w)
+    q_lens = [7, 12, 25, 16]  # longer than contexts 3, 9, 20, equal to 16
+    q, cu = _queries_over_pool(w, q_lens, 22)
+    out, lse = oracle.paged_attention(q, kp, vp, w.block_tables, w.context_lens, cu, w.scale,
+                                      causal=False)
+    G = w.num_q_heads // w.num_kv_heads
+    for s in range(w.num_seqs):
+        k, v = logical_kv(w, s)
+        K = k.double().permute(1, 0, 2).repeat_interleave(G, 0)[None]
+        V = v.double().permute(1, 0, 2).repeat_interleave(G, 0)[None]
+        r0, r1 = int(cu[s]), int(cu[s + 1])
+        Q = q[r0:r1].double().permute(1, 0, 2)[None]
+        ref = F.scaled_dot_product_attention(Q, K, V, scale=w.scale)[0].permute(1, 0, 2)
+        ref_lse = torch.logsumexp((Q @ K.transpose(-1, -2)) * w.scale, -1)[0].permute(1, 0)
+        np.testing.assert_allclose(out[r0:r1], ref.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[r0:r1], ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+    # rows of one sequence share one context: with equal queries they agree
+    q2 = q.clone()
+    q2[int(cu[2]):int(cu[3])] = q[int(cu[2])]
+    out2, _ = oracle.paged_attention(q2, kp, vp, w.block_tables, w.context_lens, cu, w.scale,
+                                     causal=False)
+    assert np.all(out2[int(cu[2]):int(cu[3])] == out2[int(cu[2])])
+
+
+def test_causal_window_longer_than_context_is_rejected():
+    # a causal query j sits at position c - Lq + j, which is negative for
+    # Lq > c: no such window exists, and the oracle refuses it (as it refuses
+    # any non-empty window over an empty context)
+    w = W.build("nc", 23, [3, 9], [1, 1], pool_factor=1.5, num_q_heads=4, num_kv_heads=2,
+                head_dim=8, block_size=4)
+    kp, vp = oracle_pools(w)
+    q, cu = _queries_over_pool(w, [4, 2], 24)
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_attention(q, kp, vp, w.block_tables, w.context_lens, cu, w.scale,
+                               causal=True)
+    cl0 = w.context_lens.clone()
+    cl0[1] = 0
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_attention(q, kp, vp, w.block_tables, cl0, cu, w.scale, causal=False)
