@@ -1,29 +1,37 @@
 """Benchmark: paged decode attention on GB300 (tokens/s and HBM GB/s).
 
-One step = one attention layer's decode step of the engine-shaped batch
-(64 sequences, context 384, q_len 1, 16 query / 8 KV heads, head_dim 128,
-block 16, bf16): the slot-mapped write of the 64 new tokens' K/V into the
-block pool, then paged decode attention over the pool (balanced split with
-its merge) -- one ``pa_append_decode`` call (three kernels). Inputs are device resident when the timed region starts; the
-e2e figure instead moves each step's inputs from pinned host memory and
-reads the result back, through the library's public calls.
+Headline workload: the ragged continuous batch -- 256 sequences, q_len 1,
+context lengths log-uniform in 1..4096, 30% of the sequences sharing a
+refcounted 512-token prefix (the same physical blocks), 16 query / 8 KV
+heads, head_dim 128, block 16, bf16, pool 1.2x the blocks needed. One step is
+one attention layer's decode step: the slot-mapped write of the 256 new
+tokens' K/V into the block pool, then paged decode attention over the pool
+(balanced split with its merge) -- one ``pa_append_decode`` call (three
+kernels). Inputs are device resident when the timed region starts; the e2e
+figure moves each step's inputs from pinned host memory and reads the result
+back, through the library's public calls.
 
-The KV pool of the engine batch (100.7 MB) is smaller than the 129 MB L2, so
-the benchmark keeps several layers' caches (as a model has) and rotates
-through them step by step: each step reads a pool that the previous steps
-have pushed out of L2.
+A model has one KV cache per layer, so the benchmark keeps 28 layers' pools
+(the Qwen3-0.6B shape) and each step reads the next layer's pool: no step
+finds the previous step's pool in L2. Steps are replayed from CUDA graphs of
+up to 28 steps each, so the per-step figure does not depend on ``--steps``.
+
+The same measurement (device-timed steps, the decode call's roofline, e2e,
+and the fp64 oracle timed on the host cores) is repeated for the engine batch
+(64 x 384) and the long-context batch (8 x 32768, balanced and split-K
+16/32/64) under ``secondary``, together with the verify + chunked-prefill
+call, the INT8 pool and the cascade decode.
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
 torchrun, each rank runs its own replica batch (the path shards by sequence
 with no exchange) and rank 0 prints one JSON line. ``--impl reference`` times
-the fp64 CPU oracle on the same workload instead.
+the fp64 CPU oracle on the headline workload instead.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -38,41 +46,64 @@ import torch  # noqa: E402
 
 METRIC = ("paged decode attention tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU")
 UNIT = "tokens/s"
-WORKLOAD = ("engine-shaped decode: batch 64, q_len 1, every context 384, 16 Q / 8 KV heads, "
-            "head_dim 128, block 16, bf16, shuffled pool; step = cache write of 64 new "
-            "tokens + paged decode attention")
-LAYERS = 28                     # one KV cache per layer of the Qwen3-0.6B shape (28 x 100.7 MB)
+LAYERS = 28                     # one KV cache per layer of the Qwen3-0.6B shape
+GRAPH_STEPS = 28                # steps per captured graph (fewer when --steps is smaller)
 FALLBACK_HBM_GBS = 6800.0       # only if MEASURED_PEAKS.json is missing
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
+WORKLOADS = {
+    "ragged": ("ragged continuous batch: batch 256, q_len 1, context lengths log-uniform "
+               "1-4096, 30% of sequences share a refcounted 512-token prefix, 16 Q / 8 KV "
+               "heads, head_dim 128, block 16, bf16, pool 1.2x the blocks needed; step = "
+               "cache write of 256 new tokens + paged decode attention"),
+    "engine": ("engine-shaped decode: batch 64, q_len 1, every context 384, 16 Q / 8 KV heads, "
+               "head_dim 128, block 16, bf16, shuffled pool; step = cache write of 64 new "
+               "tokens + paged decode attention"),
+    "long": ("long-context decode: batch 8, q_len 1, context 32768 each, 16 Q / 8 KV heads, "
+             "head_dim 128, block 16, bf16, 1% outlier keys x8; step = cache write of 8 new "
+             "tokens + paged decode attention (balanced split)"),
+    "mixed": ("mixed verify + chunked prefill: 48 sequences with q_len 5 at contexts "
+              "256-8192 + 2 prefill chunks of 512 queries at offsets 0 and 1536, causal, "
+              "16 Q / 8 KV heads, head_dim 128, block 16, bf16"),
+}
+HEADLINE = "ragged"
+
 
 # ---------------------------------------------------------------------------
-# helpers
+# byte and flop counts
 # ---------------------------------------------------------------------------
 
-def decode_algorithmic_bytes(w) -> int:
+def decode_algorithmic_bytes(w, unique: bool = False, kv_bytes_per_token: int | None = None) -> int:
     """Bytes one decode call must move at least: every context token's K and V
     for all KV heads (4096 B per token at 8 x 128 bf16), q in, out and lse
-    out, context lengths and the block-table entries it reads."""
+    out, context lengths and the block-table entries it reads. unique: a
+    shared prefix's rows are counted once (its physical blocks are the same
+    for every sharer, so HBM has to deliver them only once per call)."""
     ctx = w.context_lens.to(torch.int64)
-    kv = int(ctx.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    tokens = int(ctx.sum())
+    if unique:
+        for seqs, t in w.meta.get("prefix_groups", []):
+            tokens -= t * (len(seqs) - 1)
+    per_tok = kv_bytes_per_token or w.num_kv_heads * w.head_dim * 2 * 2
     S, Hq, D = w.num_seqs, w.num_q_heads, w.head_dim
     rows = w.num_q_tokens
     q_out = rows * Hq * D * 2 * 2 + rows * Hq * 4
     tables = int(((ctx + w.block_size - 1) // w.block_size).sum()) * 4 + S * 4
-    return kv + q_out + tables
+    return tokens * per_tok + q_out + tables
 
 
-def decode_algorithmic_bytes_int8(w) -> int:
-    """As decode_algorithmic_bytes for the int8 pool: 1-byte K and V codes plus
-    one fp32 scale per (token, KV head) row each (2112 B per token)."""
-    ctx = w.context_lens.to(torch.int64)
-    kv = int(ctx.sum()) * w.num_kv_heads * (w.head_dim + 4) * 2
-    S, Hq, D = w.num_seqs, w.num_q_heads, w.head_dim
-    rows = w.num_q_tokens
-    q_out = rows * Hq * D * 2 * 2 + rows * Hq * 4
-    tables = int(((ctx + w.block_size - 1) // w.block_size).sum()) * 4 + S * 4
-    return kv + q_out + tables
+def int8_bytes_per_token(w) -> int:
+    """int8 pool: 1-byte K and V codes plus one fp32 scale per (token, KV head)
+    row each (2112 B per token at 8 x 128)."""
+    return w.num_kv_heads * (w.head_dim + 4) * 2
+
+
+def attention_flops(w) -> int:
+    """Useful flops of one call: 4 * D per (query row, head, visible key)."""
+    n = 0
+    for c, l in zip(w.context_lens.tolist(), w.q_lens.tolist()):
+        n += sum(c - l + j + 1 for j in range(l)) if w.causal else l * c
+    return n * 4 * w.head_dim * w.num_q_heads
 
 
 def peaks():
@@ -94,8 +125,8 @@ def kernel_source_hash() -> str:
 
 
 def traffic_for(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current decode kernel source; else None."""
+    """DRAM bytes per pa_decode call from the committed ncu summary, if it was
+    taken on the current decode kernel source; else None."""
     try:
         d = json.load(open(TRAFFIC_FILE))
         e = d.get(workload)
@@ -123,6 +154,13 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 def whole_job_rate(tokens_per_step: int, steps: int, world: int, max_total_ms: float) -> float:
     """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
     return world * tokens_per_step * steps / (max_total_ms / 1e3)
+
+
+def graph_plan(K: int, chunk: int = GRAPH_STEPS):
+    """Split K steps into graph replays of at most `chunk` steps: (steps per
+    full graph, number of full replays, steps of the remainder graph)."""
+    c = max(1, min(K, chunk))
+    return c, K // c, K % c
 
 
 class ClockSampler:
@@ -189,146 +227,182 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# our arm
+# timing helpers
 # ---------------------------------------------------------------------------
 
-class Layer:
-    """One layer's KV pool (filled by the CUDA cache write) and its graphs."""
-
-    def __init__(self, w, dev, B, bufs):
-        self.kc, self.vc = w.empty_pool(dev)
-        if w.k_hist.shape[0]:
-            B.pa_reshape_and_cache(bufs["k_hist"], bufs["v_hist"], bufs["slot_hist"],
-                                   self.kc, self.vc)
-        B.pa_reshape_and_cache(bufs["k_new"], bufs["v_new"], bufs["slot_new"], self.kc,
-                               self.vc)
+def capture(fn, n: int, first: int = 0):
+    """A CUDA graph of n calls fn(first), fn(first + 1), ... ."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(first, first + n):
+            fn(i)
+    return g
 
 
-def run_ours(args, rank, world, dev):
-    from paged_kv_decode_18_gb300 import binding as B
-    from paged_kv_decode_18_gb300 import workloads as W
-
-    B.load()
-    w = W.engine(seed=replica_seed(args.seed, rank))
-    stream = torch.cuda.current_stream()
-    bufs = {k: getattr(w, k).to(dev) for k in
-            ("q", "k_new", "v_new", "slot_new", "k_hist", "v_hist", "slot_hist",
-             "block_tables", "context_lens")}
-    layers = [Layer(w, dev, B, bufs) for _ in range(LAYERS)]
-    out = torch.empty_like(bufs["q"])
-    lse = torch.empty(bufs["q"].shape[:2], dtype=torch.float32, device=dev)
-    sh = B.shape_of(bufs["q"], layers[0].kc, bufs["block_tables"])
-    ws = B.workspace(B.pa_decode_workspace_size(sh, 0), dev)
+def timed_replays(graphs, stream):
+    """CUDA-event time (ms) of each graph replay, in order, on `stream`."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in graphs]
+    chunk = 128
+    for c0 in range(0, len(graphs), chunk):
+        # park the stream briefly so the host can queue a chunk of replays ahead
+        torch.cuda._sleep(2_000_000)
+        for i in range(c0, min(len(graphs), c0 + chunk)):
+            ev[i][0].record(stream)
+            graphs[i].replay()
+            ev[i][1].record(stream)
     torch.cuda.synchronize()
-    if B.pa_debug_read_error() != 0:
-        raise RuntimeError("device error while filling the pools")
+    return [a.elapsed_time(b) for a, b in ev]
 
-    def step(l):
-        # the whole step in one call: cache write of the new tokens, then decode
-        B.pa_append_decode(bufs["k_new"], bufs["v_new"], bufs["slot_new"], bufs["q"], l.kc, l.vc,
-                           bufs["block_tables"], bufs["context_lens"], w.scale, out, lse,
-                           workspace=ws)
 
-    def decode(l):
-        B.pa_decode(bufs["q"], l.kc, l.vc, bufs["block_tables"], bufs["context_lens"],
-                    w.scale, out, lse, num_splits=0, workspace=ws)
+def mean_call_ms(fn, n_layers: int, reps: int, stream, per_graph: int = GRAPH_STEPS):
+    """Mean time of one call when `per_graph` calls (rotating over n_layers
+    inputs) run back to back in one graph."""
+    fn(0)
+    g = capture(lambda i: fn(i % n_layers), per_graph)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    ms = timed_replays([g] * reps, stream)
+    return statistics.fmean(ms) / per_graph, statistics.median(ms) / per_graph
 
-    # CUDA graphs, as an engine captures its decode step: one graph runs the
-    # attention step of every layer of the model back to back, each layer on
-    # its own KV cache (graph launch cost is paid once per replay, not per
-    # layer); single-layer graphs cover a remainder.
+
+# ---------------------------------------------------------------------------
+# one decode workload on the device
+# ---------------------------------------------------------------------------
+
+class DecodeBench:
+    """A decode workload's inputs on the device and `layers` KV pools, each
+    filled by the CUDA cache write (history, then the step's new tokens)."""
+
+    def __init__(self, w, dev, B, layers):
+        self.w, self.dev, self.B = w, dev, B
+        names = ("q", "k_new", "v_new", "slot_new", "block_tables", "context_lens")
+        self.d = {k: getattr(w, k).to(dev) for k in names}
+        kh, vh, sh_ = w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev)
+        self.pools = []
+        for _ in range(layers):
+            kc, vc = w.empty_pool(dev)
+            if w.k_hist.shape[0]:
+                B.pa_reshape_and_cache(kh, vh, sh_, kc, vc)
+            B.pa_reshape_and_cache(self.d["k_new"], self.d["v_new"], self.d["slot_new"], kc, vc)
+            self.pools.append((kc, vc))
+        del kh, vh, sh_
+        self.out = torch.empty_like(self.d["q"])
+        self.lse = torch.empty(self.d["q"].shape[:2], dtype=torch.float32, device=dev)
+        self.shape = B.shape_of(self.d["q"], self.pools[0][0], self.d["block_tables"])
+        self.ws = {}
+        torch.cuda.synchronize()
+        if B.pa_debug_read_error() != 0:
+            raise RuntimeError("device error while filling the pools")
+
+    def workspace(self, P):
+        if P not in self.ws:
+            self.ws[P] = self.B.workspace(self.B.pa_decode_workspace_size(self.shape, P), self.dev)
+        return self.ws[P]
+
+    def step_calls(self):
+        """One prepared pa_append_decode call per layer pool."""
+        d, w = self.d, self.w
+        return [self.B.prepare_append_decode(d["k_new"], d["v_new"], d["slot_new"], d["q"], kc, vc,
+                                             d["block_tables"], d["context_lens"], w.scale,
+                                             self.out, self.lse, workspace=self.workspace(0))
+                for kc, vc in self.pools]
+
+    def decode_calls(self, P):
+        d, w = self.d, self.w
+        return [self.B.prepare_decode(d["q"], kc, vc, d["block_tables"], d["context_lens"],
+                                      w.scale, self.out, self.lse, num_splits=P,
+                                      workspace=self.workspace(P))
+                for kc, vc in self.pools]
+
+
+def measure_decode(name, w, dev, B, args, layers, splits=(0,), world=1, clocks=None,
+                   e2e=True):
+    """Device-timed steps (exactly args.steps), the decode call's roofline for
+    each split mode, and the e2e step through host buffers."""
+    stream = torch.cuda.current_stream()
+    bench = DecodeBench(w, dev, B, layers)
+    n = len(bench.pools)
+    steps = bench.step_calls()
+    step = lambda i: steps[i % n]()  # noqa: E731
+    K = args.steps
+    chunk, full, rem = graph_plan(K)
+    # warm the plain calls up once outside capture (first-call setup)
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        for l in layers:
-            step(l)
-            decode(l)
+        for i in range(n):
+            step(i)
     stream.wait_stream(side)
-
-    def capture(fn, ls):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for l in ls:
-                fn(l)
-        return g
-
-    g_steps = capture(step, layers)
-    g_decs = capture(decode, layers)
-    g_step1 = [capture(step, [l]) for l in layers]
+    g_full = capture(step, chunk)
+    g_rem = capture(step, rem, first=chunk) if rem else None
     torch.cuda.synchronize()
-
-    clocks = ClockSampler(torch.cuda.current_device() if dev.index is None else dev.index)
-    clocks.start()
-    for _ in range(max(1, args.warmup // LAYERS)):
-        g_steps.replay()
-        g_decs.replay()
+    for _ in range(max(1, -(-args.warmup // chunk))):
+        g_full.replay()
     torch.cuda.synchronize()
-
-    def timed(graphs):
-        """CUDA-event time (ms) of each graph replay, in order."""
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in graphs]
-        chunk = 128
-        for c0 in range(0, len(graphs), chunk):
-            # park the stream briefly so the host can queue a chunk of replays ahead
-            torch.cuda._sleep(2_000_000)
-            for i in range(c0, min(len(graphs), c0 + chunk)):
-                ev[i][0].record(stream)
-                graphs[i].replay()
-                ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in ev]
-
-    K = args.steps
-    plan = [g_steps] * (K // LAYERS) + g_step1[:K % LAYERS]   # exactly K steps
+    plan = [g_full] * full + ([g_rem] if g_rem is not None else [])
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.mark()
-    step_ms = timed(plan)
-    clocks.mark()
+    if clocks is not None:
+        clocks.mark()
+    step_ms = timed_replays(plan, stream)
+    if clocks is not None:
+        clocks.mark()
     if world > 1:
         torch.distributed.barrier()
-    # the dominant call on its own, for the roofline: mean time per call of
-    # LAYERS back-to-back decode calls in one graph
-    dec_rep = timed([g_decs] * max(1, min(K, 2000) // LAYERS))
-    dec_ms = [t / LAYERS for t in dec_rep]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
-    clk = clocks.stop()
+
+    peak, peak_kind = peaks()
+    alg = decode_algorithmic_bytes(w, unique=True)
+    alg_logical = decode_algorithmic_bytes(w)
+    reps = max(3, min(K, 2000) // GRAPH_STEPS)
+    rooflines = {}
+    for P in splits:
+        calls = bench.decode_calls(P)
+        mean_ms, med_ms = mean_call_ms(lambda i: calls[i % n](), n, reps, stream)
+        achieved = alg / (mean_ms / 1e3) / 1e9
+        rooflines[P] = {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic_for(name) if P == 0 else None,
+            "kernel": ("pa_decode (paged_decode_kernel + decode_fixup_kernel)" if P == 0 else
+                       f"pa_decode num_splits={P} (paged_decode_kernel + splitk_reduce_kernel)"),
+            "alg_bytes_per_launch": alg, "alg_bytes_logical": alg_logical,
+            "achieved_logical": round(alg_logical / (mean_ms / 1e3) / 1e9, 1),
+            "launch_ms": round(mean_ms, 5), "launch_ms_median": round(med_ms, 5),
+            "peak_source": f"{peak_kind} hbm_gbs",
+        }
     err = B.pa_debug_read_error()
     if err != 0:
-        raise RuntimeError(f"device error word {err:#x} after the timed region")
-
-    tokens_per_step = w.num_q_tokens
-    value = whole_job_rate(tokens_per_step, K, world, total_ms)
-    dec_mean_ms = statistics.fmean(dec_ms)
-    alg = decode_algorithmic_bytes(w)
-    peak, peak_kind = peaks()
-    achieved = alg / (dec_mean_ms / 1e3) / 1e9
+        raise RuntimeError(f"device error word {err:#x} after the timed region ({name})")
     res = {
-        "value": value,
+        "workload": WORKLOADS.get(name, name),
+        "value": whole_job_rate(w.num_q_tokens, K, world, total_ms),
         "ms_per_step": total_ms / K,
-        "decode_ms": dec_mean_ms,
-        "decode_ms_median": statistics.median(dec_ms),
-        "alg_bytes": alg,
-        "achieved": achieved,
-        "peak": peak,
-        "peak_kind": peak_kind,
-        "clocks": clk,
-        "launches": 3 * K,   # cache write, decode, merge per step
+        "steps": K,
+        "roofline": rooflines[splits[0]],
+        "launches": 3 * K,  # cache write, decode, merge per step
+        "l2": (f"inputs larger than L2: {n} layer pools of "
+               f"{2 * bench.pools[0][0].numel() * 2 / 1e6:.1f} MB rotated per step"),
     }
-    res["e2e"] = run_e2e(args, w, dev, B, layers, ws)
-    if rank == 0 and not args.no_secondary:
-        res["secondary"] = run_secondary(args, dev, B)
+    for P in splits[1:]:
+        res[f"roofline_splits{P}"] = rooflines[P]
+    if e2e:
+        res["e2e"] = run_e2e(args, bench)
+    del bench
+    torch.cuda.empty_cache()
     return res
 
 
-def run_e2e(args, w, dev, B, layers, ws):
-    """Same step through the public calls with host buffers: the step's inputs
+def run_e2e(args, bench):
+    """The step through the public calls with host buffers: the step's inputs
     (q, new K/V, slots, block tables, context lengths) staged in one pinned
     buffer and copied host-to-device in one copy, the library call, and out +
     lse (views of one device buffer) copied back in one copy and read on the
     host, every step."""
+    w, dev, B = bench.w, bench.dev, bench.B
     names = ("q", "k_new", "v_new", "slot_new", "block_tables", "context_lens")
 
     def packed(tensors, device, pinned):
@@ -348,113 +422,92 @@ def run_e2e(args, w, dev, B, layers, ws):
     for v, t in zip(host_views, src):
         v.copy_(t)
     dev_in, dv = packed(src, dev, False)
-    devb = dict(zip(names, dv))
+    d = dict(zip(names, dv))
     outs = [torch.empty(w.q.shape, dtype=torch.bfloat16),
             torch.empty(w.q.shape[:2], dtype=torch.float32)]
     dev_out, (out, lse) = packed(outs, dev, False)
-    host_out, (out_h, lse_h) = packed(outs, "cpu", True)
-    h2d = host_in.numel()
-    d2h = host_out.numel()
+    host_out, _ = packed(outs, "cpu", True)
+    n = len(bench.pools)
+    stream = torch.cuda.current_stream()
+
+    def prepared(st):
+        return [B.prepare_append_decode(d["k_new"], d["v_new"], d["slot_new"], d["q"], kc, vc,
+                                        d["block_tables"], d["context_lens"], w.scale, out, lse,
+                                        workspace=bench.workspace(0), stream=st)
+                for kc, vc in bench.pools]
+    calls = prepared(stream)       # eager: bound to this stream
+    calls_graph = prepared(None)   # captured: the capture stream at capture time
     steps = max(1, min(args.steps, 2000))
 
-    def step(l):
+    def step(i):
         dev_in.copy_(host_in, non_blocking=True)
-        B.pa_append_decode(devb["k_new"], devb["v_new"], devb["slot_new"], devb["q"], l.kc, l.vc,
-                           devb["block_tables"], devb["context_lens"], w.scale, out, lse,
-                           workspace=ws)
+        calls[i % n]()
         host_out.copy_(dev_out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()  # the result is read on the host
+        stream.synchronize()  # the result is read on the host
 
     for i in range(max(3, min(args.warmup, 50))):
-        step(layers[i % LAYERS])
+        step(i)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     s.record()
     for i in range(steps):
-        step(layers[i % LAYERS])
+        step(i)
     e.record()
     torch.cuda.synchronize()
     ms = s.elapsed_time(e)
     res = {"value": w.num_q_tokens * steps / (ms / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+           "h2d_bytes_per_step": host_in.numel(), "d2h_bytes_per_step": host_out.numel(),
+           "steps": steps, "ms_per_step": ms / steps,
+           "path": "prepared pa_append_decode call through the Python binding, one H2D and "
+                   "one D2H copy and a stream sync per step"}
 
     # the same step as an engine runs it: the two copies and the call captured
     # once in a CUDA graph per layer, replayed and read back every step
     graphs = []
-    for l in layers:
+    for i in range(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             dev_in.copy_(host_in, non_blocking=True)
-            B.pa_append_decode(devb["k_new"], devb["v_new"], devb["slot_new"], devb["q"], l.kc,
-                               l.vc, devb["block_tables"], devb["context_lens"], w.scale, out,
-                               lse, workspace=ws)
+            calls_graph[i]()
             host_out.copy_(dev_out, non_blocking=True)
         graphs.append(g)
     for i in range(max(3, min(args.warmup, 50))):
-        graphs[i % LAYERS].replay()
-        torch.cuda.current_stream().synchronize()
+        graphs[i % n].replay()
+        stream.synchronize()
     torch.cuda.synchronize()
     s.record()
     for i in range(steps):
-        graphs[i % LAYERS].replay()
-        torch.cuda.current_stream().synchronize()  # the result is read on the host
+        graphs[i % n].replay()
+        stream.synchronize()  # the result is read on the host
     e.record()
     torch.cuda.synchronize()
     res["graph_value"] = w.num_q_tokens * steps / (s.elapsed_time(e) / 1e3)
     return res
 
 
-def run_secondary(args, dev, B):
-    """Decode-kernel bandwidth on the other decode workloads (inputs > L2)."""
-    from paged_kv_decode_18_gb300 import workloads as W
+# ---------------------------------------------------------------------------
+# the other rows: verify + chunked prefill, int8 pool, cascade
+# ---------------------------------------------------------------------------
 
-    peak, _ = peaks()
-    res = {}
-    cases = [("ragged", W.ragged, [0]), ("long", W.long, [0, 16, 32, 64])]
-    for name, make, splits in cases:
-        w = make(seed=args.seed)
-        kc, vc = w.empty_pool(dev)
-        B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
-        B.pa_reshape_and_cache(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), kc, vc)
-        q = w.q.to(dev)
-        bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
-        out = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-        alg = decode_algorithmic_bytes(w)
-        for P in splits:
-            sh = B.shape_of(q, kc, bt)
-            ws = B.workspace(B.pa_decode_workspace_size(sh, P), dev)
-            fn = lambda: B.pa_decode(q, kc, vc, bt, cl, w.scale, out, lse, num_splits=P,  # noqa
-                                     workspace=ws)
+def time_graph_calls(fn, per_replay=2, reps=30):
+    """Mean ms of one call, `per_replay` calls per graph replay."""
+    fn()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_replay):
             fn()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):  # two calls per replay: graph launch cost halved
-                fn()
-                fn()
-            for _ in range(5):
-                g.replay()
-            n = 30
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(n)]
-            torch.cuda.synchronize()
-            torch.cuda._sleep(1_000_000)
-            for a, b in evs:
-                a.record()
-                g.replay()
-                b.record()
-            torch.cuda.synchronize()
-            ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / 2
-            gbs = alg / (ms / 1e3) / 1e9
-            res[f"{name}_splits{P}"] = {"decode_ms": round(ms, 5), "alg_bytes": alg,
-                                        "achieved_gbs": round(gbs, 1),
-                                        "frac_of_measured_peak": round(gbs / peak, 4),
-                                        "tokens_per_s": w.num_q_tokens / (ms / 1e3)}
-        del kc, vc
-        torch.cuda.empty_cache()
-    res.update(run_secondary_varlen(args, dev, B, peak))
-    res.update(run_secondary_int8(args, dev, B, peak))
-    res.update(run_secondary_cascade(args, dev, B, peak))
-    return res
+    for _ in range(5):
+        g.replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(1_000_000)
+    for a, b in evs:
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.fmean(a.elapsed_time(b) for a, b in evs) / per_replay
 
 
 def unique_kv_bytes(w) -> int:
@@ -469,18 +522,85 @@ def unique_kv_bytes(w) -> int:
             rows * w.num_q_heads * w.head_dim * 2 * 2 + rows * w.num_q_heads * 4)
 
 
-def run_secondary_cascade(args, dev, B, peak):
+def device_pool(w, dev, B):
+    kc, vc = w.empty_pool(dev)
+    B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
+    B.pa_reshape_and_cache(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), kc, vc)
+    return kc, vc
+
+
+def run_secondary_varlen(w, dev, B, peak):
+    """Verify + chunked-prefill call (tensor cores) on the mixed workload."""
+    kc, vc = device_pool(w, dev, B)
+    q = w.q.to(dev)
+    bt, cl, cu = w.block_tables.to(dev), w.context_lens.to(dev), w.cu_seqlens_q.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    sh = B.shape_of(q, kc, bt)
+    ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, q.shape[0], w.max_q_len), dev)
+    ms = time_graph_calls(lambda: B.pa_decode_varlen(q, kc, vc, bt, cl, cu, w.max_q_len, w.scale,
+                                                     out, lse, causal=True, workspace=ws))
+    alg = decode_algorithmic_bytes(w)
+    fl = attention_flops(w)
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"workload": WORKLOADS["mixed"], "call_ms": round(ms, 5), "alg_bytes": alg,
+            "achieved_gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+            "useful_gflop": round(fl / 1e9, 3),
+            "achieved_tflops": round(fl / (ms / 1e3) / 1e12, 1),
+            "value": w.num_q_tokens / (ms / 1e3), "unit": "query tokens/s"}
+
+
+def run_secondary_int8(ws_by_name, dev, B, peak):
+    """Decode over the INT8 pool (quantised cache write, fused dequant): the
+    engine batch rotated over the layer pools, the ragged and the long batch."""
+    res = {}
+    for name, nlayers in (("engine", LAYERS), ("ragged", 1), ("long", 1)):
+        w = ws_by_name[name]
+        pools = []
+        kh, vh, sh_ = w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev)
+        kn, vn, sn = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
+        for _ in range(nlayers):
+            kc, vc, ks, vs = w.empty_pool_i8(dev)
+            B.pa_reshape_and_cache_int8(kh, vh, sh_, kc, vc, ks, vs)
+            B.pa_reshape_and_cache_int8(kn, vn, sn, kc, vc, ks, vs)
+            pools.append((kc, vc, ks, vs))
+        del kh, vh, sh_
+        q = w.q.to(dev)
+        bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        sh = B.shape_of(q, pools[0][0], bt)
+        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
+        ctr = [0]
+
+        def call():
+            kc, vc, ks, vs = pools[ctr[0] % nlayers]
+            ctr[0] += 1
+            B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse, num_splits=0,
+                             workspace=ws)
+        ms = time_graph_calls(call, per_replay=4 if nlayers > 1 else 2)
+        alg = decode_algorithmic_bytes(w, unique=True, kv_bytes_per_token=int8_bytes_per_token(w))
+        gbs = alg / (ms / 1e3) / 1e9
+        res[f"{name}_int8"] = {"decode_ms": round(ms, 5), "alg_bytes": alg,
+                               "achieved_gbs": round(gbs, 1),
+                               "frac_of_measured_peak": round(gbs / peak, 4),
+                               "value": w.num_q_tokens / (ms / 1e3), "unit": UNIT,
+                               "kv_format": "int8 + fp32 row scales"}
+        del pools
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_secondary_cascade(ws_by_name, dev, B):
     """Cascade (shared-prefix) decode against plain balanced decode on the
     ragged batch (30% share a 512-token prefix) and on a shared-prompt batch
     (128 sequences behind one 4096-token prompt)."""
     from paged_kv_decode_18_gb300 import workloads as W
 
     res = {}
-    for name, make in (("ragged", W.ragged), ("shared_prompt", W.shared_prompt)):
-        w = make(seed=args.seed)
-        kc, vc = w.empty_pool(dev)
-        B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
-        B.pa_reshape_and_cache(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), kc, vc)
+    for name in ("ragged", "shared_prompt"):
+        w = ws_by_name[name]
+        kc, vc = device_pool(w, dev, B)
         q = w.q.to(dev)
         bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
         out = torch.empty_like(q)
@@ -499,205 +619,113 @@ def run_secondary_cascade(args, dev, B, peak):
         }
         ub = unique_kv_bytes(w)
         for kind, fn in calls.items():
-            fn()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn()
-                fn()
-            for _ in range(5):
-                g.replay()
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(30)]
-            torch.cuda.synchronize()
-            torch.cuda._sleep(1_000_000)
-            for a, b in evs:
-                a.record()
-                g.replay()
-                b.record()
-            torch.cuda.synchronize()
-            ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / 2
+            ms = time_graph_calls(fn)
             res[f"{name}_{kind}"] = {"call_ms": round(ms, 5), "unique_kv_bytes": ub,
                                      "unique_gbs": round(ub / (ms / 1e3) / 1e9, 1),
-                                     "tokens_per_s": w.num_q_tokens / (ms / 1e3)}
+                                     "value": w.num_q_tokens / (ms / 1e3), "unit": UNIT}
         del kc, vc
         torch.cuda.empty_cache()
     return res
 
 
-def run_secondary_int8(args, dev, B, peak):
-    """Decode over the INT8 pool (quantised cache write, fused dequant): the
-    engine batch rotated over the layer pools, the ragged and the long batch."""
-    from paged_kv_decode_18_gb300 import workloads as W
-
-    res = {}
-    for name, make, nlayers in (("engine", W.engine, LAYERS), ("ragged", W.ragged, 1),
-                                ("long", W.long, 1)):
-        w = make(seed=args.seed)
-        pools = []
-        for _ in range(nlayers):
-            kc, vc, ks, vs = w.empty_pool_i8(dev)
-            B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                        kc, vc, ks, vs)
-            B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev),
-                                        kc, vc, ks, vs)
-            pools.append((kc, vc, ks, vs))
-        q = w.q.to(dev)
-        bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
-        out = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-        sh = B.shape_of(q, pools[0][0], bt)
-        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
-
-        def call(l):
-            kc, vc, ks, vs = pools[l]
-            B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse, num_splits=0,
-                             workspace=ws)
-        per_replay = 4 if nlayers > 1 else 2
-        call(0)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(per_replay):
-                call(i % nlayers)
-        for _ in range(5):
-            g.replay()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(30)]
-        torch.cuda.synchronize()
-        torch.cuda._sleep(1_000_000)
-        for a, b in evs:
-            a.record()
-            g.replay()
-            b.record()
-        torch.cuda.synchronize()
-        ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / per_replay
-        alg = decode_algorithmic_bytes_int8(w)
-        gbs = alg / (ms / 1e3) / 1e9
-        res[f"{name}_int8"] = {"decode_ms": round(ms, 5), "alg_bytes": alg,
-                               "achieved_gbs": round(gbs, 1),
-                               "frac_of_measured_peak": round(gbs / peak, 4),
-                               "tokens_per_s": w.num_q_tokens / (ms / 1e3),
-                               "kv_format": "int8 + fp32 row scales"}
-        del pools
-        torch.cuda.empty_cache()
-    return res
-
-
-def attention_flops(w) -> int:
-    """Useful flops of one call: 4 * D per (query row, head, visible key)."""
-    n = 0
-    for c, l in zip(w.context_lens.tolist(), w.q_lens.tolist()):
-        n += sum(c - l + j + 1 for j in range(l)) if w.causal else l * c
-    return n * 4 * w.head_dim * w.num_q_heads
-
-
-def run_secondary_varlen(args, dev, B, peak):
-    """Verify + chunked-prefill call (tensor cores) on the mixed workload."""
-    from paged_kv_decode_18_gb300 import workloads as W
-
-    w = W.mixed(seed=args.seed)
-    kc, vc = w.empty_pool(dev)
-    B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
-    B.pa_reshape_and_cache(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), kc, vc)
-    q = w.q.to(dev)
-    bt, cl, cu = w.block_tables.to(dev), w.context_lens.to(dev), w.cu_seqlens_q.to(dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-    sh = B.shape_of(q, kc, bt)
-    ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, q.shape[0], w.max_q_len), dev)
-    fn = lambda: B.pa_decode_varlen(q, kc, vc, bt, cl, cu, w.max_q_len, w.scale, out, lse,  # noqa
-                                    causal=True, workspace=ws)
-    fn()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        fn()
-        fn()
-    for _ in range(5):
-        g.replay()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(20)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(1_000_000)
-    for a, b in evs:
-        a.record()
-        g.replay()
-        b.record()
-    torch.cuda.synchronize()
-    ms = statistics.fmean(a.elapsed_time(b) for a, b in evs) / 2
-    alg = decode_algorithmic_bytes(w)
-    fl = attention_flops(w)
-    gbs = alg / (ms / 1e3) / 1e9
-    return {"mixed_varlen": {"call_ms": round(ms, 5), "alg_bytes": alg, "achieved_gbs": round(gbs, 1),
-                             "frac_of_measured_peak": round(gbs / peak, 4), "useful_gflop": round(fl / 1e9, 3),
-                             "achieved_tflops": round(fl / (ms / 1e3) / 1e12, 1),
-                             "query_tokens_per_s": w.num_q_tokens / (ms / 1e3)}}
-
-
 # ---------------------------------------------------------------------------
-# the oracle on the host cores (cpu_baseline leg and --impl reference)
+# the oracle on the host cores (cpu_baseline legs and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_rate(seed: int, budget_s: float, max_steps: int | None = None,
-                num_threads: int = 0):
-    """Time the fp64 oracle on the engine workload: each step is the oracle's
-    cache write of the new tokens plus paged attention over a sample of the
-    sequences (num_threads 0 = all host cores). Returns (tokens/s, threads,
-    description, steps, seqs/step)."""
+def subset_workload(w, seqs):
+    """The sequences `seqs` of a workload with their rows of q / new K/V:
+    index bookkeeping only."""
+    import copy
+
+    idx = torch.tensor(seqs, dtype=torch.int64)
+    cu = w.cu_seqlens_q.to(torch.int64)
+    rows = torch.cat([torch.arange(int(cu[s]), int(cu[s + 1])) for s in seqs])
+    sub = copy.copy(w)
+    sub.context_lens = w.context_lens[idx]
+    sub.q_lens = w.q_lens[idx]
+    sub.block_tables = w.block_tables[idx]
+    sub.q, sub.k_new, sub.v_new, sub.slot_new = (w.q[rows], w.k_new[rows], w.v_new[rows],
+                                                 w.slot_new[rows])
+    c = torch.zeros(len(seqs) + 1, dtype=torch.int32)
+    c[1:] = torch.cumsum(sub.q_lens, 0)
+    sub.cu_seqlens_q = c
+    return sub
+
+
+def oracle_rate(w, budget_s: float, num_threads: int = 0, max_steps: int | None = None,
+                name: str = ""):
+    """Time the fp64 oracle on a workload: each step is the oracle's cache
+    write of the new tokens plus paged attention over a sample of the
+    sequences (the whole batch when one step fits a third of the budget,
+    else evenly spaced sequences sized to that). num_threads 0 = all host
+    cores. Returns (query tokens/s, threads, description, steps, tokens per step)."""
     import numpy as np
 
     from oracle import oracle
     from paged_kv_decode_18_gb300 import workloads as W
 
-    w = W.engine(seed=seed)
     kp = np.full(w.pool_shape(), W.POOL_SENTINEL_BITS, np.uint16)
     vp = kp.copy()
-    oracle.reshape_and_cache(w.k_hist, w.v_hist, w.slot_hist, kp, vp, w.block_size)
+    if w.k_hist.shape[0]:
+        oracle.reshape_and_cache(w.k_hist, w.v_hist, w.slot_hist, kp, vp, w.block_size)
     threads = oracle.max_threads() if num_threads <= 0 else num_threads
 
-    def one(n_seqs):
-        oracle.reshape_and_cache(w.k_new[:n_seqs], w.v_new[:n_seqs], w.slot_new[:n_seqs], kp, vp,
-                                 w.block_size)
-        oracle.paged_attention(w.q[:n_seqs], kp, vp, w.block_tables[:n_seqs],
-                               w.context_lens[:n_seqs], w.cu_seqlens_q[:n_seqs + 1], w.scale,
-                               num_threads=threads)
+    def one(x):
+        oracle.reshape_and_cache(x.k_new, x.v_new, x.slot_new, kp, vp, x.block_size)
+        oracle.paged_attention(x.q, kp, vp, x.block_tables, x.context_lens, x.cu_seqlens_q,
+                               x.scale, causal=x.causal, num_threads=threads)
 
     t = time.perf_counter()
-    one(w.num_seqs)
+    one(w)
     full = time.perf_counter() - t
-    n_seqs = w.num_seqs
-    if max_steps is not None:
-        per_step = budget_s / max(1, max_steps)
-        n_seqs = max(1, min(w.num_seqs, int(w.num_seqs * per_step / max(full, 1e-6))))
+    per_step = budget_s / 3 if max_steps is None else budget_s / max(1, max_steps)
+    x = w
+    if full > per_step and w.num_seqs > 1:
+        n = max(1, min(w.num_seqs, int(w.num_seqs * per_step / max(full, 1e-6))))
+        seqs = sorted(set(np.linspace(0, w.num_seqs - 1, n).round().astype(int).tolist()))
+        x = subset_workload(w, seqs)
     steps = 0
-    tokens = 0
     t0 = time.perf_counter()
     while True:
-        one(n_seqs)
+        one(x)
         steps += 1
-        tokens += n_seqs
         el = time.perf_counter() - t0
         if max_steps is not None and steps >= max_steps:
             break
         if max_steps is None and el >= budget_s and steps >= 3:
             break
     el = time.perf_counter() - t0
-    desc = (f"fp64 oracle, engine workload: {steps} steps of cache write + paged attention "
-            f"over {n_seqs} of 64 sequences (context 384), {threads} threads")
-    return tokens / el, threads, desc, steps, n_seqs
+    what = "all" if x is w else "an evenly spaced sample"
+    desc = (f"fp64 oracle, {name or w.name} workload: {steps} steps of cache write + paged "
+            f"attention over {what} {x.num_seqs} of {w.num_seqs} sequences "
+            f"({x.num_q_tokens} query tokens per step), {threads} threads")
+    return x.num_q_tokens * steps / el, threads, desc, steps, x.num_q_tokens
+
+
+def cpu_baseline(w, name, budget_all=6.0, budget_one=2.0):
+    rate, threads, desc, _, _ = oracle_rate(w, budget_all, name=name)
+    rate1, _, desc1, _, _ = oracle_rate(w, budget_one, num_threads=1, name=name)
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+            "value_1_thread": rate1, "sample_1_thread": desc1}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    budget = 120.0
-    # warm-up steps, then exactly K timed steps sized to fit the budget
-    oracle_rate(args.seed, 5.0, max_steps=max(3, args.warmup))
-    rate, threads, desc, steps, n = oracle_rate(args.seed, budget, max_steps=args.steps)
+    from paged_kv_decode_18_gb300 import workloads as W
+
+    w = W.make(HEADLINE, seed=args.seed)
+    budget = 100.0
+    per = budget / (args.steps + max(3, args.warmup))
+    oracle_rate(w, per * max(3, args.warmup), max_steps=max(3, args.warmup), name=HEADLINE)
+    rate, threads, desc, steps, n = oracle_rate(w, per * args.steps, max_steps=args.steps,
+                                                name=HEADLINE)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * n / rate,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "num_seqs": 64, "context_len": 384,
+        "config": {"workload": WORKLOADS[HEADLINE], "num_seqs": w.num_seqs,
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
@@ -720,13 +748,13 @@ def run_case(args, dev):
     B.load()
     if args.case == "prefill":  # the chunked-prefill part of the mixed batch
         w = W.mixed(seed=args.seed, num_verify=0)
-    elif args.case == "ragged_int8":
-        w = W.ragged(seed=args.seed)
+    elif args.case in ("ragged_int8", "engine_int8", "long_int8"):
+        w = W.make(args.case[:-5], seed=args.seed)
     elif args.case == "shared_prompt":
         w = W.shared_prompt(seed=args.seed)
     else:
         w = W.make(args.case, seed=args.seed)
-    int8 = args.case == "ragged_int8"
+    int8 = args.case.endswith("_int8")
     if int8:
         kc, vc, ks, vs = w.empty_pool_i8(dev)
         B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
@@ -784,28 +812,62 @@ def run_case(args, dev):
     err = B.pa_debug_read_error()
     ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
     print(json.dumps({"case": args.case, "splits": args.splits, "step_ms": ms,
-                      "alg_bytes": decode_algorithmic_bytes(w), "device_error": err}))
+                      "alg_bytes": decode_algorithmic_bytes(w),
+                      "alg_bytes_unique": decode_algorithmic_bytes(w, unique=True),
+                      "device_error": err}))
     return 1 if err else 0
 
 
 # ---------------------------------------------------------------------------
 
+def run_ours(args, rank, world, dev):
+    from paged_kv_decode_18_gb300 import binding as B
+    from paged_kv_decode_18_gb300 import workloads as W
+
+    B.load()
+    peak, _ = peaks()
+    clocks = ClockSampler(torch.cuda.current_device() if dev.index is None else dev.index)
+    clocks.start()
+    w = W.make(HEADLINE, seed=replica_seed(args.seed, rank))
+    head = measure_decode(HEADLINE, w, dev, B, args, LAYERS, world=world, clocks=clocks)
+    clk = clocks.stop()
+    head["clocks"] = clk
+    if rank != 0 or args.no_secondary:
+        return head, None, {HEADLINE: w}
+    sec = {}
+    ws_by_name = {HEADLINE: w}
+    for name, layers, splits in (("engine", LAYERS, (0,)), ("long", 2, (0, 16, 32, 64))):
+        wx = W.make(name, seed=args.seed)
+        ws_by_name[name] = wx
+        sec[name] = measure_decode(name, wx, dev, B, args, layers, splits=splits)
+    wm = W.mixed(seed=args.seed)
+    ws_by_name["mixed"] = wm
+    sec["mixed_varlen"] = run_secondary_varlen(wm, dev, B, peak)
+    sec.update(run_secondary_int8(ws_by_name, dev, B, peak))
+    ws_by_name["shared_prompt"] = W.shared_prompt(seed=args.seed)
+    sec.update(run_secondary_cascade(ws_by_name, dev, B))
+    return head, sec, ws_by_name
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=280)
+    ap.add_argument("--warmup", type=int, default=28)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["tiny", "engine", "ragged", "long", "mixed", "prefill",
-                                       "ragged_int8", "shared_prompt"],
+                                       "ragged_int8", "engine_int8", "long_int8",
+                                       "shared_prompt"],
                     help="time one workload with eager calls (for profiling), nothing else")
     ap.add_argument("--splits", type=int, default=0, help="num_splits for --case decode runs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -825,47 +887,42 @@ def main():
     if world > 1:
         torch.distributed.barrier()
 
-    r = run_ours(args, rank, world, dev)
+    head, sec, ws_by_name = run_ours(args, rank, world, dev)
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline:
-            rate, threads, desc, _, _ = oracle_rate(args.seed, 10.0)
-            rate1, _, desc1, _, _ = oracle_rate(args.seed, 3.0, num_threads=1)
-            cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                   "sample": desc, "value_1_thread": rate1, "sample_1_thread": desc1}
-        traffic = traffic_for("engine")
+            cpu = cpu_baseline(ws_by_name[HEADLINE], HEADLINE)
+            if sec is not None:
+                for name in ("engine", "long"):
+                    sec[name]["cpu_baseline"] = cpu_baseline(ws_by_name[name], name)
+                sec["mixed_varlen"]["cpu_baseline"] = cpu_baseline(ws_by_name["mixed"], "mixed")
+        w = ws_by_name[HEADLINE]
         line = {
             "metric": METRIC,
-            "value": r["value"],
+            "value": head["value"],
             "unit": UNIT,
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": r["ms_per_step"],
+            "ms_per_step": head["ms_per_step"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "num_seqs": 64, "context_len": 384,
-                       "global_batch": 64 * world, "parallelism": f"replicas x{world}",
-                       "num_splits": 0,
-                       "l2": f"inputs larger than L2: {LAYERS} layer caches of 100.7 MB "
-                             "rotated per step"},
-            "roofline": {"bound": "hbm", "achieved": round(r["achieved"], 1),
-                         "peak": r["peak"], "unit": "GB/s",
-                         "frac": round(r["achieved"] / r["peak"], 4), "traffic": traffic,
-                         "kernel": "pa_decode (paged_decode_kernel + decode_fixup_kernel)",
-                         "alg_bytes_per_launch": r["alg_bytes"],
-                         "launch_ms": round(r["decode_ms"], 5),
-                         "peak_source": f"{r['peak_kind']} hbm_gbs"},
+            "config": {"workload": WORKLOADS[HEADLINE], "num_seqs": w.num_seqs,
+                       "context_tokens": int(w.context_lens.sum()),
+                       "global_batch": w.num_seqs * world, "parallelism": f"replicas x{world}",
+                       "num_splits": 0, "l2": head["l2"],
+                       "graph_steps": graph_plan(args.steps)[0]},
+            "roofline": head["roofline"],
             "cpu_baseline": cpu,
-            "e2e": r["e2e"],
-            "gpu_launches": r["launches"],
-            "clocks": r["clocks"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["launches"],
+            "clocks": head["clocks"],
         }
-        if "secondary" in r:
-            line["secondary"] = r["secondary"]
+        if sec is not None:
+            line["secondary"] = sec
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -320,8 +320,33 @@ def pa_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_
            "pa_decode_int8")
 
 
-def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
-              num_splits: int = 0, workspace=None, stream=None) -> None:
+def _prepared(cfn, args, stream, what, keep):
+    """A zero-argument callable that makes one C-ABI call with arguments that
+    were checked and converted once (the tensors in `keep` stay referenced).
+    The stream goes last: fixed now when one was given, else the current
+    torch stream at each call (so the call can also be captured in a graph)."""
+    if stream is not None:
+        full = args + (_stream(stream),)
+
+        def call():
+            rc = cfn(*full)
+            if rc != PA_OK:
+                raise PAError(rc, what)
+    else:
+        def call():
+            rc = cfn(*args, _stream(None))
+            if rc != PA_OK:
+                raise PAError(rc, what)
+    call.keep = keep
+    return call
+
+
+def prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
+                   num_splits: int = 0, workspace=None, stream=None):
+    """pa_decode with its arguments checked and marshalled now; the returned
+    callable makes the call each time it is invoked, on `stream` if one is
+    given, else on the torch stream current at that moment. For serving loops
+    that issue the same call on fixed buffers."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -336,16 +361,23 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=N
     if out.shape != q.shape:
         raise ValueError("out shape != q shape")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                            _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
-                            ctypes.byref(sh), int(num_splits), _ptr(workspace), ws_bytes,
-                            _stream(stream)), "pa_decode")
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+            ctypes.c_float(scale), _ptr(out), _ptr(lse), ctypes.byref(sh),
+            ctypes.c_int(num_splits), _ptr(workspace), ctypes.c_size_t(ws_bytes))
+    keep = (q, k_cache, v_cache, block_tables, context_lens, out, lse, workspace, sh)
+    return _prepared(load().pa_decode, args, stream, "pa_decode", keep)
 
 
-def pa_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
-                     context_lens, scale, out, lse=None, workspace=None, stream=None) -> None:
-    """Cache write of the step's new K/V rows, then decode (balanced split), as
-    one call whose decode preparation overlaps the write."""
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
+              num_splits: int = 0, workspace=None, stream=None) -> None:
+    prepare_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse,
+                   num_splits, workspace, stream)()
+
+
+def prepare_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                          context_lens, scale, out, lse=None, workspace=None, stream=None):
+    """pa_append_decode with its arguments checked and marshalled now (see
+    prepare_decode)."""
     _need(k_new, "k_new", torch.bfloat16, 3)
     _need(v_new, "v_new", torch.bfloat16, 3)
     _need(slot_mapping, "slot_mapping", torch.int64, 1)
@@ -365,11 +397,21 @@ def pa_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tabl
     if out.shape != q.shape:
         raise ValueError("out shape != q shape")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pa_append_decode(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0],
-                                   _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                   _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
-                                   ctypes.byref(sh), _ptr(workspace), ws_bytes,
-                                   _stream(stream)), "pa_append_decode")
+    args = (_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), ctypes.c_int64(k_new.shape[0]),
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+            ctypes.c_float(scale), _ptr(out), _ptr(lse), ctypes.byref(sh), _ptr(workspace),
+            ctypes.c_size_t(ws_bytes))
+    keep = (k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables, context_lens, out,
+            lse, workspace, sh)
+    return _prepared(load().pa_append_decode, args, stream, "pa_append_decode", keep)
+
+
+def pa_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                     context_lens, scale, out, lse=None, workspace=None, stream=None) -> None:
+    """Cache write of the step's new K/V rows, then decode (balanced split), as
+    one call whose decode preparation overlaps the write."""
+    prepare_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                          context_lens, scale, out, lse, workspace, stream)()
 
 
 def pa_decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale, out,
