@@ -175,12 +175,13 @@ int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new, const int64_t* 
  * cudaMalloc would also synchronise the device).
  *
  * Arguments, layouts and results are those of pa_decode. The split scratch is
- * a fixed 4 MiB array inside the library (static device memory that every GPU
+ * a fixed 8 MiB array inside the library (static device memory that every GPU
  * loading the library holds until the process exits). A shape whose balanced
- * split needs more than 4 MiB on the current device returns PA_ERR_WORKSPACE
- * (use pa_decode with a workspace instead); on a 152-SM GB300 the need is
- * about 2.5 MiB for any batch. The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
+ * split needs more than 8 MiB on the current device returns PA_ERR_WORKSPACE
+ * (use pa_decode with a workspace instead); the need is 2 partial slots x 2
+ * heads x 129 fp32 per resident warp of the decode grid: 3.6 MiB on a 152-SM
+ * GB300, for any batch. The first call in each CUDA context looks up the
+ * array's device address (cudaGetSymbolAddress) with that context current;
  * make that first call before any stream capture. All calls share the one
  * array and its contents carry over between calls (nothing in it needs to
  * start at zero): calls that may overlap on the GPU -- on different streams,

@@ -417,7 +417,7 @@ def pa_append_decode(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tabl
 def pa_decode_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                              lse=None, stream=None) -> None:
     """pa_decode (balanced split) without a workspace, for callers that cannot
-    allocate device memory: the split scratch is a fixed 4 MiB array inside the
+    allocate device memory: the split scratch is a fixed 8 MiB array inside the
     library. Calls that may overlap on the GPU share that array and race."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)

@@ -24,7 +24,8 @@
 //     packed f32x2 FMA pipe of sm_100+;
 //   * online softmax in the log2 domain (scale * log2 e folded into q);
 //   * PV: the same lane layout accumulates 2 heads x 16 dims in fp32 pairs;
-//     the 4 token groups are combined through shared memory once per piece.
+//     the 4 token groups are combined by a shuffle reduce-scatter once per
+//     piece, after the stage has been refilled.
 // A batch is cut into equal tile ranges over all resident warps (num_splits
 // 0), so ragged batches and long contexts balance; a (sequence, KV head) cut
 // by a range boundary leaves partials that a small merge kernel combines.
@@ -544,69 +545,65 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
       }
     }
     __syncwarp();  // all lanes are done with this stage's K/V and with pbuf
+    // refill the stage now: finishing a piece below needs no stage memory, so
+    // its work overlaps the copy
+    if (pidx < R1) issue(stage);
 
     const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
     if (last) {
-      // ---- finish the piece: combine the 4 token groups through this stage's
-      // (already consumed) K/V buffers, 4 KB, then each lane owns 8 outputs ----
-      float* red = reinterpret_cast<float*>(st);  // [grp][g][128] fp32 = 4 KB
+      // ---- finish the piece: sum the 4 token groups' accumulators (lanes
+      // c8, c8+8, c8+16, c8+24) by a reduce-scatter over lane bits 4 and 3;
+      // lane (b4, b3, c8) ends with head b4, dims 16*c8 + 8*b3 .. +7 ----------
+      const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+      float h16[16];  // after lane bit 4: head b4, dims 16*c8 .. 16*c8+15
 #pragma unroll
-      for (int g = 0; g < kG; ++g) {
-        float4* dst = reinterpret_cast<float4*>(red + (grp * kG + g) * kHeadDim + c8 * 16);
+      for (int j = 0; j < 8; ++j) {
+        const float2 mine = b4 ? acc[1][j] : acc[0][j];
+        const float2 send = b4 ? acc[0][j] : acc[1][j];
+        h16[2 * j] = mine.x + __shfl_xor_sync(kFull, send.x, 16);
+        h16[2 * j + 1] = mine.y + __shfl_xor_sync(kFull, send.y, 16);
+      }
+      float o8[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dst[j] = make_float4(acc[g][2 * j].x, acc[g][2 * j].y, acc[g][2 * j + 1].x,
-                               acc[g][2 * j + 1].y);
+      for (int i = 0; i < 8; ++i) {
+        const float mine = b3 ? h16[8 + i] : h16[i];
+        const float send = b3 ? h16[i] : h16[8 + i];
+        o8[i] = mine + __shfl_xor_sync(kFull, send, 8);
       }
       float ls = l_lane;
 #pragma unroll
       for (int o = 2; o < 32; o <<= 1) ls += __shfl_xor_sync(kFull, ls, o);
       const float lo = __shfl_xor_sync(kFull, ls, 1);
       const float l0 = hsel ? lo : ls, l1 = hsel ? ls : lo;
-      __syncwarp();
-      const int og = lane >> 4;          // output head of this lane
-      const int od = (lane & 15) * 8;    // output dims od .. od+7
-      float o8[8];
-      {
-        const float4* r0 = reinterpret_cast<const float4*>(red + og * kHeadDim + od);
-        float4 x = r0[0], y = r0[1];
-#pragma unroll
-        for (int gg = 1; gg < 4; ++gg) {
-          const float4* r = reinterpret_cast<const float4*>(red + (gg * kG + og) * kHeadDim + od);
-          const float4 u = r[0], v = r[1];
-          x.x += u.x; x.y += u.y; x.z += u.z; x.w += u.w;
-          y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
-        }
-        o8[0] = x.x; o8[1] = x.y; o8[2] = x.z; o8[3] = x.w;
-        o8[4] = y.x; o8[5] = y.y; o8[6] = y.z; o8[7] = y.w;
-      }
+      const int og = b4 ? 1 : 0;             // output head of this lane
+      const int od = c8 * 16 + (b3 ? 8 : 0);  // output dims od .. od+7
       const float lsum = og ? l1 : l0;
       const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
       const float inv = 1.f / lsum;
       const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
       const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
+      const bool lse_lane = (lane & 15) == 0;
       if (a.mode == kFixed && a.num_splits > 1) {
         const int PS = a.num_splits;
         store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
-        if ((lane & 15) == 0) a.part_lse[row * PS + fixed_p] = lse_own;
+        if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
       } else if (complete && a.rows.o) {
         const size_t r = row * a.rows.stride + a.rows.slot;
         store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
-        if ((lane & 15) == 0) a.rows.lse[r] = lse_own;
+        if (lse_lane) a.rows.lse[r] = lse_own;
       } else if (complete) {
         store_out8(a.out + row * kHeadDim + od, o8, inv);
-        if (a.lse && (lane & 15) == 0) a.lse[row] = lse_own;
+        if (a.lse && lse_lane) a.lse[row] = lse_own;
       } else {
         const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
         store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
-        if ((lane & 15) == 0) a.part_lse[slot * kG + og] = lse_own;
+        if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
       }
-      __syncwarp();  // the reduction buffer is read before the refill lands
     }
 
-    if (pidx < R1) issue(stage);
     if (idx + 1 < R1) advance(P, S, Hkv, cp);
   }
+
   late_exit();
 }
 
@@ -712,7 +709,11 @@ constexpr int kWarpsLong = 8;
 constexpr int kStages = 2;    // bf16: 2 x 8 KB of copies in flight per warp
 constexpr int kStagesQ8 = 3;  // int8: 3 x 4 KB (two CTAs per SM still fit)
 
+struct DecodeGeometry;
+using DecodeLaunch = cudaError_t (*)(const DecodeGeometry&, const DecodeArgs&, cudaStream_t);
+
 struct DecodeGeometry {
+  DecodeLaunch launch = nullptr;  // the decode grid of this shape
   int mode = kBalanced;
   int P = 0;
   int grid = 0;
@@ -721,16 +722,27 @@ struct DecodeGeometry {
   size_t fixup_smem = 0;
   size_t ws_desc = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
   int nwarps = kWarps;  // warps per CTA of the decode grid
+  int nstages = kStages;  // stages per warp
+};
+
+// A CTA shape of the decode grid: NW warps of NST stages, pool format Q8.
+template <bool Q8, int NW, int NST>
+struct DecodeShape {
+  static cudaError_t launch(const DecodeGeometry& g, const DecodeArgs& a, cudaStream_t st) {
+    return launch_dependent(paged_decode_kernel<NW, NST, Q8>, dim3(g.grid), dim3(NW * 32), g.smem,
+                            st, a);
+  }
 };
 
 inline size_t plan_smem_bytes(int S) { return sizeof(int) * (4 * (size_t)S + 3 + 40); }
 
 // max_sms > 0: size the balanced grid for that many SMs (the rest are busy).
-template <bool Q8, int NW>
+template <bool Q8, int NW, int NST>
 int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int max_sms = 0) {
-  constexpr int NST = Q8 ? kStagesQ8 : kStages;
   constexpr int kWarps = NW;
   g->nwarps = NW;
+  g->nstages = NST;
+  g->launch = &DecodeShape<Q8, NW, NST>::launch;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
@@ -770,13 +782,13 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int
 
 int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool q8 = false,
                     int max_sms = 0) {
-  if (q8) return decode_geometry_t<true, kWarps>(sh, num_splits, g, max_sms);
+  if (q8) return decode_geometry_t<true, kWarps, kStagesQ8>(sh, num_splits, g, max_sms);
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const bool long_ctx = num_splits == 0 && max_sms == 0 &&
                         (int64_t)sh->num_seqs * sh->num_kv_heads <= dev.num_sms;
-  return long_ctx ? decode_geometry_t<false, kWarpsLong>(sh, num_splits, g, max_sms)
-                  : decode_geometry_t<false, kWarps>(sh, num_splits, g, max_sms);
+  return long_ctx ? decode_geometry_t<false, kWarpsLong, kStages>(sh, num_splits, g, max_sms)
+                  : decode_geometry_t<false, kWarps, kStages>(sh, num_splits, g, max_sms);
 }
 
 int check_decode_args(const pa_shape* shape, int num_splits) {
@@ -890,15 +902,7 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
   a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
 
-  const cudaError_t le =
-      q8 ? launch_dependent(paged_decode_kernel<kWarps, kStagesQ8, true>, dim3(g.grid),
-                            dim3(kWarps * 32), g.smem, st, a)
-      : g.nwarps == kWarpsLong
-          ? launch_dependent(paged_decode_kernel<kWarpsLong, kStages, false>, dim3(g.grid),
-                             dim3(kWarpsLong * 32), g.smem, st, a)
-          : launch_dependent(paged_decode_kernel<kWarps, kStages, false>, dim3(g.grid),
-                             dim3(kWarps * 32), g.smem, st, a);
-  if (le != cudaSuccess) return PA_ERR_CUDA;
+  if (g.launch(g, a, st) != cudaSuccess) return PA_ERR_CUDA;
   const int wpb = 8;
   if (g.mode == kBalanced) {
     // the merge grid may be scheduled while the decode grid drains; it waits
@@ -1027,30 +1031,59 @@ extern "C" int pa_splitk_reduce(const float* part_out, const float* part_lse, in
 namespace pa {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+// 8 MiB. The balanced split needs 2 partial slots x 2 heads x 129 fp32 per
+// resident warp: 3.6 MiB on a 152-SM GB300 (1824 warps), so the array covers
+// devices of up to about 300 SMs at this CTA shape.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_pa_static_scratch[kStaticScratchBytes];
 
-// Device address of the scratch array on the current device. In host code the
+// Device address of the scratch array in the current context. In host code the
 // array's name is only a host-side stand-in, so the real address is looked up
-// once per device (with that device current) and cached.
+// (cudaGetSymbolAddress, with the device current) the first time a context
+// calls, and cached per context: a new context on the same device (after a
+// device reset, for instance) looks it up again.
 void* static_scratch_address(int* rc) {
-  static std::mutex mu;
-  static void* addr[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  using GetCtx = CUresult (*)(CUcontext*);
+  static GetCtx get_ctx = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<GetCtx>(p);
+  });
+  if (get_ctx == nullptr) {
     *rc = PA_ERR_CUDA;
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || p == nullptr) {
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) == CUDA_SUCCESS && ctx == nullptr) {
+    // no context on this thread yet: the runtime creates the device's primary
+    // context at its first call that needs one
+    if (cudaFree(nullptr) != cudaSuccess) {
       *rc = PA_ERR_CUDA;
       return nullptr;
     }
-    addr[dev] = p;
+    get_ctx(&ctx);
   }
-  return addr[dev];
+  if (ctx == nullptr) {
+    *rc = PA_ERR_CUDA;
+    return nullptr;
+  }
+  static std::mutex mu;
+  static std::map<CUcontext, void*> addr;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = addr.find(ctx);
+  if (it != addr.end()) return it->second;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || p == nullptr) {
+    *rc = PA_ERR_CUDA;
+    return nullptr;
+  }
+  addr[ctx] = p;
+  return p;
 }
 
 }  // namespace
