@@ -130,8 +130,11 @@ int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v, const int64_t* slot
  *                      warp, and merges the pieces of sequences that were cut;
  *                 1  = no split: one warp per (sequence, KV head);
  *                 P >= 2 = every (sequence, KV head) is cut into P near-equal
- *                      block ranges whose partials are merged by
- *                      pa_splitk_reduce (P <= 1024).
+ *                      block ranges (partitions; P <= 1024); each partition's
+ *                      normalised output and log-sum-exp are merged with the
+ *                      pa_splitk_reduce formula (empty partitions weigh
+ *                      nothing). The partitions' tiles are spread over the
+ *                      resident warps like num_splits 0 does with sequences.
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
  *                 bytes, 256-byte aligned; may be NULL when that size is 0.
  *                 Its contents need no initialisation and are clobbered.

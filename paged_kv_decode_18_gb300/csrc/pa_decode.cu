@@ -80,6 +80,8 @@ struct DecodeArgs {
   int mode;         // kBalanced or kFixed
   int num_splits;   // kFixed: P
   int num_workers;  // kBalanced: warps launched
+  int parts;        // kBalanced: split-K partitions per sequence (1: none); with
+                    // parts > 1 finished partitions go to `rows` in slot = partition
   float* part_o;    // kBalanced: [NW*2][G][D]; kFixed: [S][Hq][P][D]
   float* part_lse;  // kBalanced: [NW*2][G];    kFixed: [S][Hq][P]
   int early;        // 1: plan and table reads may run before the previous grid ends
@@ -249,9 +251,10 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
   const int S = a.S, Hkv = a.Hkv, Hq = a.Hq;
 
   int* pm = reinterpret_cast<int*>(smem + NWARPS * L::kBytes);
+  const int parts = a.mode == kBalanced ? a.parts : 1;
   PlanSmem P;
   P.pair_off = pm;
-  P.seq_pair = P.pair_off + (S + 1);
+  P.seq_pair = P.pair_off + (S * parts + 1);
   P.ctx = P.seq_pair + (S + 1);
   P.qstart = P.ctx + S;
   int* scratch = P.qstart + (S + 1);
@@ -281,8 +284,9 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
   in.max_ctx = a.max_blocks * kBlock;
   in.qtile = 1;
   in.causal = 1;
-  in.npairs_cap = S;
+  in.npairs_cap = S * parts;
   in.num_q_rows = S;
+  in.parts = parts;
   build_plan(in, P, scratch);  // ends with __syncthreads: barrier inits visible too
   bool waited = !a.early || a.late;
   if (a.early && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -302,13 +306,16 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
 
   // Sequences with an empty context: out = 0, lse = -inf (balanced mode owns
   // them in CTA 0; fixed mode handles them through its empty partials).
-  if (a.mode == kBalanced && blockIdx.x == 0) {
-    for (int s = warp; s < S; s += NWARPS) {
-      if (P.ctx[s] != 0) continue;
+  // (With split-K partitions, empty ones are skipped by the partition merge.)
+  if (a.mode == kBalanced && parts == 1 && blockIdx.x == 0) {
+    for (int pr = warp; pr < P.npairs; pr += NWARPS) {
+      if (P.pair_off[pr + 1] != P.pair_off[pr]) continue;
+      const int s = pr / parts;
+      const int rslot = a.rows.slot;
       for (int h = 0; h < Hq; ++h) {
         const size_t row = (size_t)s * Hq + h;
         if (a.rows.o) {
-          const size_t r = row * a.rows.stride + a.rows.slot;
+          const size_t r = row * a.rows.stride + rslot;
           *reinterpret_cast<float4*>(a.rows.o + r * kHeadDim + lane * 4) =
               make_float4(0.f, 0.f, 0.f, 0.f);
           if (lane == 0) a.rows.lse[r] = neg_inf();
@@ -368,10 +375,14 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
   int pidx = R0;
   int wbase = R0;
   // block id of flat tile idx; tiles of a window lie a few pairs past pp
+  // block of the sequence that tile t reads (its partition's first block + b)
+  auto abs_block = [&](const TilePos& t) -> int {
+    return parts > 1 ? t.b + part_begin(t.qt, (P.ctx[t.s] + kBlock - 1) / kBlock, parts) : t.b;
+  };
   auto load_phys = [&](int idx) -> int {
     if (idx >= R1) return 0;
     const TilePos t = locate_from(P, Hkv, pp, idx);
-    return a.block_tables[(size_t)t.s * a.max_blocks + t.b];
+    return a.block_tables[(size_t)t.s * a.max_blocks + abs_block(t)];
   };
   int phys_cur = load_phys(wbase + lane);
   int phys_next = load_phys(wbase + 32 + lane);
@@ -456,7 +467,7 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
       piece_b0 = cp.b;
       piece_first = (idx == R0);
     }
-    const int nvalid = min(kBlock, P.ctx[cp.s] - cp.b * kBlock);
+    const int nvalid = min(kBlock, P.ctx[cp.s] - abs_block(cp) * kBlock);
 
     // ---- scores: 4 tokens x 2 heads of partial dots per lane ----------------
     float sc[8];
@@ -588,7 +599,7 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
         store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
         if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
       } else if (complete && a.rows.o) {
-        const size_t r = row * a.rows.stride + a.rows.slot;
+        const size_t r = row * a.rows.stride + (parts > 1 ? cp.qt : a.rows.slot);
         store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
         if (lse_lane) a.rows.lse[r] = lse_own;
       } else if (complete) {
@@ -616,7 +627,7 @@ __global__ void __launch_bounds__(NWARPS * 32, NWARPS <= 6 ? 2 : 1)
 // the partial vectors of a round are loaded together.
 __global__ void __launch_bounds__(256)
     decode_fixup_kernel(const int32_t* __restrict__ context_lens, int S, int Hkv, int max_blocks,
-                        int num_workers, const float* __restrict__ part_o,
+                        int num_workers, int parts, const float* __restrict__ part_o,
                         const float* __restrict__ part_lse, int Hq, uint16_t* __restrict__ out,
                         float* __restrict__ lse, const RowsOut rows) {
   // the next grid in the stream may start its own preparation now; it waits
@@ -625,7 +636,7 @@ __global__ void __launch_bounds__(256)
   extern __shared__ __align__(16) int fx_smem[];
   PlanSmem P;
   P.pair_off = fx_smem;
-  P.seq_pair = P.pair_off + (S + 1);
+  P.seq_pair = P.pair_off + (S * parts + 1);
   P.ctx = P.seq_pair + (S + 1);
   P.qstart = P.ctx + S;
   PlanInputs in;
@@ -636,8 +647,9 @@ __global__ void __launch_bounds__(256)
   in.max_ctx = max_blocks * kBlock;
   in.qtile = 1;
   in.causal = 1;
-  in.npairs_cap = S;
+  in.npairs_cap = S * parts;
   in.num_q_rows = S;
+  in.parts = parts;
   build_plan(in, P, nullptr);
   const int W = P.total;
   const int nw = min(num_workers, W);
@@ -646,7 +658,9 @@ __global__ void __launch_bounds__(256)
   const MergeJob job = merge_job(P, S, Hkv, w, W, nw);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!job.valid) return;
-  merge_segment(job, w, lane, part_o, part_lse, Hq, out, lse, rows);
+  RowsOut r = rows;
+  if (parts > 1) r.slot = job.qt;  // the partition's partial slot
+  merge_segment(job, w, lane, part_o, part_lse, Hq, out, lse, r);
 }
 
 // Split-K merge over a regular [rows][heads][P][D] partial layout: one warp
@@ -697,6 +711,122 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part_o,
   if (lse && lane == 0) lse[rh] = LSE;
 }
 
+// The split-K merge of decode partitions: the a7 formula over the [S][Hq][P]
+// partials, where partition j of sequence s counts only if it holds blocks
+// (part_begin(j) < part_begin(j + 1) for the sequence's context), so empty
+// partitions are never written or read. A CTA has kPrWarps warps; RW of them
+// share one (sequence, head) row: warp k of a row merges partitions k, k + RW,
+// ... with the loads of a round of kMergeChunk partitions in flight together,
+// then the row's warps combine their (max, sum, vector) through shared memory.
+constexpr int kPrWarps = 8;
+
+template <int RW>
+__global__ void __launch_bounds__(kPrWarps * 32)
+    parts_reduce_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                        const int32_t* __restrict__ context_lens, int max_ctx, int64_t nrh,
+                        int Hq, int P, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  __shared__ float sm_m[kPrWarps], sm_l[kPrWarps];
+  __shared__ float4 sm_acc[kPrWarps][32];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = wid % RW;  // warp within the row
+  const int64_t rh = (int64_t)blockIdx.x * (kPrWarps / RW) + wid / RW;
+  if (rh >= nrh) return;  // whole rows leave together (RW divides kPrWarps)
+  const int s = (int)(rh / Hq);
+  const int c = min(max(context_lens[s], 0), max_ctx);
+  const int nt = (c + kBlock - 1) / kBlock;
+  const float* L = part_lse + rh * P;
+  const float* O = part_o + rh * (int64_t)P * kHeadDim;
+  float mx = neg_inf(), sum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // this warp's partitions: j = warp + RW * i
+  const int mine = (P - warp + RW - 1) / RW;
+  for (int i0 = 0; i0 < mine; i0 += kMergeChunk) {
+    const int n = min(kMergeChunk, mine - i0);
+    bool use[kMergeChunk];
+    float li = neg_inf();
+    float4 o[kMergeChunk];
+#pragma unroll
+    for (int k = 0; k < kMergeChunk; ++k) {
+      const int j = warp + RW * (i0 + k);
+      use[k] = k < n && part_begin(j, nt, P) < part_begin(j + 1, nt, P);
+      o[k] = use[k] ? *reinterpret_cast<const float4*>(O + (int64_t)j * kHeadDim + lane * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == k && use[k]) li = L[j];
+    }
+    float m = li;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
+    m = fmaxf(m, mx);
+    if (m == neg_inf()) continue;  // nothing in this round, nor before
+    const float r = ex2((mx - m) * kLog2e);
+    sum *= r;
+    acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+    const float e = ex2((li - m) * kLog2e);  // weight of partition lane (0 if unused)
+    float t = e;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) t += __shfl_xor_sync(kFull, t, x);
+    sum += t;
+    mx = m;
+#pragma unroll
+    for (int k = 0; k < kMergeChunk; ++k) {
+      const float wt = __shfl_sync(kFull, e, k);
+      if (use[k]) {
+        acc.x = fmaf(wt, o[k].x, acc.x);
+        acc.y = fmaf(wt, o[k].y, acc.y);
+        acc.z = fmaf(wt, o[k].z, acc.z);
+        acc.w = fmaf(wt, o[k].w, acc.w);
+      }
+    }
+  }
+  if (RW > 1) {
+    if (lane == 0) {
+      sm_m[wid] = mx;
+      sm_l[wid] = sum;
+    }
+    sm_acc[wid][lane] = acc;
+    // the row's warps meet (a named barrier per row group)
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + wid / RW), "r"(RW * 32) : "memory");
+    if (warp != 0) return;
+  }
+  const int w0 = wid;  // the row's first warp
+  float M = neg_inf();
+  if (RW > 1) {
+#pragma unroll
+    for (int k = 0; k < RW; ++k) M = fmaxf(M, sm_m[w0 + k]);
+  } else {
+    M = mx;
+  }
+  uint16_t* orow = out + rh * kHeadDim;
+  if (M == neg_inf()) {  // every partition empty: an empty context
+    *reinterpret_cast<uint2*>(orow + lane * 4) = make_uint2(0u, 0u);
+    if (lse && lane == 0) lse[rh] = neg_inf();
+    return;
+  }
+  float l = sum;
+  float4 v = acc;
+  if (RW > 1) {
+    l = 0.f;
+    v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < RW; ++k) {
+      if (sm_m[w0 + k] == neg_inf()) continue;
+      const float wk = ex2((sm_m[w0 + k] - M) * kLog2e);
+      l = fmaf(wk, sm_l[w0 + k], l);
+      const float4 ak = sm_acc[w0 + k][lane];
+      v.x = fmaf(wk, ak.x, v.x);
+      v.y = fmaf(wk, ak.y, v.y);
+      v.z = fmaf(wk, ak.z, v.z);
+      v.w = fmaf(wk, ak.w, v.w);
+    }
+  }
+  const float inv = 1.f / l;
+  uint2 ob;
+  ob.x = pack_bf2(v.x * inv, v.y * inv);
+  ob.y = pack_bf2(v.z * inv, v.w * inv);
+  *reinterpret_cast<uint2*>(orow + lane * 4) = ob;
+  if (lse && lane == 0) lse[rh] = M + lg2(l) * kLn2;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -720,7 +850,8 @@ struct DecodeGeometry {
   int workers = 0;
   size_t smem = 0;
   size_t fixup_smem = 0;
-  size_t ws_desc = 0, ws_lse = 0, ws_o = 0, ws_bytes = 0;
+  size_t ws_desc = 0, ws_lse = 0, ws_o = 0, ws_plse = 0, ws_po = 0, ws_bytes = 0;
+  int parts = 1;  // balanced: split-K partitions per sequence
   int nwarps = kWarps;  // warps per CTA of the decode grid
   int nstages = kStages;  // stages per warp
 };
@@ -734,9 +865,16 @@ struct DecodeShape {
   }
 };
 
-inline size_t plan_smem_bytes(int S) { return sizeof(int) * (4 * (size_t)S + 3 + 40); }
+// shared memory of the plan: pair_off [S * parts + 1], seq_pair [S + 1], ctx [S],
+// qstart [S + 1], and 40 spare ints
+inline size_t plan_smem_bytes(int S, int parts = 1) {
+  return sizeof(int) * ((size_t)S * parts + 1 + 3 * (size_t)S + 2 + 40);
+}
 
 // max_sms > 0: size the balanced grid for that many SMs (the rest are busy).
+// num_splits 0: balanced cut of the sequences' tiles; P >= 2: balanced cut of
+// the tiles of P partitions per sequence when their plan fits in shared
+// memory (the kFixed layout of one warp per partition otherwise); 1: kFixed.
 template <bool Q8, int NW, int NST>
 int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int max_sms = 0) {
   constexpr int kWarps = NW;
@@ -746,25 +884,34 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
-  g->smem = (size_t)kWarps * WarpLayout<NST, Q8>::kBytes + plan_smem_bytes(S);
-  if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
   const void* kern = reinterpret_cast<const void*>(paged_decode_kernel<NW, NST, Q8>);
   if (!raise_smem_limit(kern)) return PA_ERR_CUDA;
-  if (num_splits == 0) {
+  const size_t warp_bytes = (size_t)kWarps * WarpLayout<NST, Q8>::kBytes;
+  const int parts = num_splits >= 2 ? num_splits : 1;
+  if (num_splits != 1 && warp_bytes + plan_smem_bytes(S, parts) <= (size_t)dev.max_smem_optin) {
+    g->smem = warp_bytes + plan_smem_bytes(S, parts);
     int per_sm = 0;
     if (!kernel_occupancy(kern, kWarps * 32, g->smem, &per_sm) || per_sm <= 0)
       return PA_ERR_CUDA;
     g->mode = kBalanced;
+    g->parts = parts;
+    g->P = num_splits;
     g->grid = (max_sms > 0 && max_sms < dev.num_sms ? max_sms : dev.num_sms) * per_sm;
     g->workers = g->grid * kWarps;
-    g->fixup_smem = plan_smem_bytes(S);
+    g->fixup_smem = plan_smem_bytes(S, parts);
     if (g->fixup_smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
     if (g->fixup_smem > 48 * 1024 &&
         !raise_smem_limit(reinterpret_cast<const void*>(decode_fixup_kernel)))
       return PA_ERR_CUDA;
     g->ws_lse = round_up(sizeof(float) * 2 * kG * (size_t)g->workers, 256);
     g->ws_o = round_up(sizeof(float) * 2 * kG * kHeadDim * (size_t)g->workers, 256);
+    if (parts > 1) {  // the partitions' partials, merged by pa_splitk_reduce
+      g->ws_plse = round_up(sizeof(float) * (size_t)S * Hq * parts, 256);
+      g->ws_po = round_up(sizeof(float) * (size_t)S * Hq * parts * kHeadDim, 256);
+    }
   } else {
+    g->smem = warp_bytes + plan_smem_bytes(S);
+    if (g->smem > (size_t)dev.max_smem_optin) return PA_ERR_UNSUPPORTED;
     g->mode = kFixed;
     g->P = num_splits;
     const int64_t warps = (int64_t)S * Hkv * num_splits;
@@ -776,7 +923,7 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int
       g->ws_o = round_up(sizeof(float) * (size_t)S * Hq * num_splits * kHeadDim, 256);
     }
   }
-  g->ws_bytes = g->ws_desc + g->ws_lse + g->ws_o;
+  g->ws_bytes = g->ws_desc + g->ws_lse + g->ws_o + g->ws_plse + g->ws_po;
   return PA_OK;
 }
 
@@ -785,7 +932,7 @@ int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool 
   if (q8) return decode_geometry_t<true, kWarps, kStagesQ8>(sh, num_splits, g, max_sms);
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
-  const bool long_ctx = num_splits == 0 && max_sms == 0 &&
+  const bool long_ctx = num_splits != 1 && max_sms == 0 &&
                         (int64_t)sh->num_seqs * sh->num_kv_heads <= dev.num_sms;
   return long_ctx ? decode_geometry_t<false, kWarpsLong, kStages>(sh, num_splits, g, max_sms)
                   : decode_geometry_t<false, kWarps, kStages>(sh, num_splits, g, max_sms);
@@ -889,18 +1036,31 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   a.mode = g.mode;
   a.num_splits = g.P;
   a.num_workers = g.workers;
+  a.parts = g.parts;
   a.early = early;
   a.late = late;
   if (late && (early || g.mode != kBalanced)) return PA_ERR_ARG;
   a.skip_copy = g_inject_missing_copy;
   g_inject_missing_copy = -1;
   if (rows) {
-    if (g.mode != kBalanced || !rows->o || !rows->lse) return PA_ERR_ARG;
+    if (g.mode != kBalanced || g.parts > 1 || !rows->o || !rows->lse) return PA_ERR_ARG;
     a.rows = *rows;
   }
   char* ws = static_cast<char*>(workspace);
   a.part_lse = g.ws_lse ? reinterpret_cast<float*>(ws + g.ws_desc) : nullptr;
   a.part_o = g.ws_o ? reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse) : nullptr;
+  float* plse = nullptr;
+  float* po = nullptr;
+  if (g.parts > 1) {
+    // finished partitions land as fp32 partials [S][Hq][P], slot = partition
+    plse = reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse + g.ws_o);
+    po = reinterpret_cast<float*>(ws + g.ws_desc + g.ws_lse + g.ws_o + g.ws_plse);
+    a.rows.o = po;
+    a.rows.lse = plse;
+    a.rows.stride = g.parts;
+    a.rows.slot = 0;
+    a.rows.tokens = a.S;
+  }
 
   if (g.launch(g, a, st) != cudaSuccess) return PA_ERR_CUDA;
   const int wpb = 8;
@@ -909,9 +1069,28 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
     // for the decode grid's completion before reading
     if (launch_dependent(decode_fixup_kernel, dim3((g.workers + wpb - 1) / wpb), dim3(wpb * 32),
                          g.fixup_smem, st, context_lens, a.S, a.Hkv, a.max_blocks, g.workers,
-                         (const float*)a.part_o, (const float*)a.part_lse, a.Hq, (uint16_t*)out,
-                         lse, a.rows) != cudaSuccess)
+                         g.parts, (const float*)a.part_o, (const float*)a.part_lse, a.Hq,
+                         (uint16_t*)out, lse, a.rows) != cudaSuccess)
       return PA_ERR_CUDA;
+    if (g.parts > 1) {  // the split-K merge of the P partitions
+      const int64_t nrh = (int64_t)a.S * a.Hq;
+      // warps per row: one round of up to 8 partitions each
+      const int rw = g.parts >= 64 ? 8 : g.parts >= 32 ? 4 : g.parts >= 16 ? 2 : 1;
+      const unsigned blocks = (unsigned)((nrh * rw + kPrWarps - 1) / kPrWarps);
+      const int mctx = a.max_blocks * kBlock;
+      if (rw == 8)
+        parts_reduce_kernel<8><<<blocks, kPrWarps * 32, 0, st>>>(po, plse, context_lens, mctx,
+                                                                  nrh, a.Hq, g.parts, out, lse);
+      else if (rw == 4)
+        parts_reduce_kernel<4><<<blocks, kPrWarps * 32, 0, st>>>(po, plse, context_lens, mctx,
+                                                                  nrh, a.Hq, g.parts, out, lse);
+      else if (rw == 2)
+        parts_reduce_kernel<2><<<blocks, kPrWarps * 32, 0, st>>>(po, plse, context_lens, mctx,
+                                                                  nrh, a.Hq, g.parts, out, lse);
+      else
+        parts_reduce_kernel<1><<<blocks, kPrWarps * 32, 0, st>>>(po, plse, context_lens, mctx,
+                                                                  nrh, a.Hq, g.parts, out, lse);
+    }
   } else if (g.P > 1) {
     const int64_t nrh = (int64_t)a.S * a.Hq;
     splitk_reduce_kernel<<<(unsigned)((nrh + wpb - 1) / wpb), wpb * 32, 0, st>>>(

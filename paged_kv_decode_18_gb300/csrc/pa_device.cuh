@@ -211,7 +211,16 @@ struct PlanInputs {
   int key_tile = kBlock;       // keys per flat tile (a multiple of the block size)
   int min_lq = 0;              // sequences whose q_len lies outside [min_lq, max_lq]
   int max_lq = 0x7fffffff;     // belong to another kernel: no tiles here (not an error)
+  // decode only: every sequence is cut into `parts` near-equal block ranges,
+  // one pair each (pair s * parts + j holds blocks part_begin(j) ..), the
+  // split-K partitions; 1 = one pair per sequence
+  int parts = 1;
 };
+
+// First block of partition j of a sequence with nt blocks cut into `parts`.
+__device__ __forceinline__ int part_begin(int j, int nt, int parts) {
+  return (int)(((long long)j * nt) / parts);
+}
 
 // Exclusive scan of n ints in shared memory, in place, by warp 0 of the CTA
 // (each lane scans a contiguous chunk, then the lanes' totals are scanned by
@@ -277,7 +286,7 @@ __device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scra
       P.qstart[s] = q0;
       P.seq_pair[s] = (lq + in.qtile - 1) / in.qtile;  // query tiles of s
       if (s == S - 1) P.qstart[S] = in.cu_seqlens_q[S];
-    } else {
+    } else if (in.parts <= 1) {
       P.qstart[s] = s;
       P.seq_pair[s] = s;
       P.pair_off[s] = in.Hkv * ((c + kBlock - 1) / kBlock);
@@ -285,10 +294,21 @@ __device__ inline void build_plan(const PlanInputs& in, PlanSmem& P, int* /*scra
         P.qstart[S] = S;
         P.seq_pair[S] = S;
       }
+    } else {
+      const int nt = (c + kBlock - 1) / kBlock;
+      P.qstart[s] = s;
+      P.seq_pair[s] = s * in.parts;
+      for (int j = 0; j < in.parts; ++j)
+        P.pair_off[s * in.parts + j] =
+            in.Hkv * (part_begin(j + 1, nt, in.parts) - part_begin(j, nt, in.parts));
+      if (s == S - 1) {
+        P.qstart[S] = S;
+        P.seq_pair[S] = S * in.parts;
+      }
     }
   }
   __syncthreads();
-  int npairs = S;
+  int npairs = varlen || in.parts <= 1 ? S : S * in.parts;
   if (varlen) {
     if (tid < 32) {
       const int n = warp0_exclusive_scan(P.seq_pair, S);
