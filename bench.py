@@ -614,8 +614,12 @@ def run_secondary_cascade(ws_by_name, dev, B):
         calls = {
             "decode": lambda: B.pa_decode(q, kc, vc, bt, cl, w.scale, out, lse,  # noqa
                                           num_splits=0, workspace=wsd),
+            # the library's choice (PA_CASCADE_AUTO), and the cascade's phases forced
             "cascade": lambda: B.pa_decode_cascade(q, kc, vc, bt, cl, sg, cu, mem, pl, mg,  # noqa
                                                    mp, w.scale, out, lse, workspace=wsc),
+            "cascade_forced": lambda: B.pa_decode_cascade(  # noqa
+                q, kc, vc, bt, cl, sg, cu, mem, pl, mg, mp, w.scale, out, lse, workspace=wsc,
+                policy=B.PA_CASCADE_ALWAYS),
         }
         ub = unique_kv_bytes(w)
         for kind, fn in calls.items():

@@ -314,6 +314,15 @@ size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_splits);
  * A description that breaks these rules sets PA_DEVERR_QLEN_RANGE or
  * PA_DEVERR_CONTEXT_RANGE; the output is then unspecified. Built for
  * num_q_heads == 2 * num_kv_heads (as pa_decode).
+ *
+ * pa_decode_cascade chooses between the cascade and plain pa_decode
+ * (PA_CASCADE_AUTO below): the cascade's extra phases (gathering the members'
+ * queries, the prefix tile, two merges) pay only when the prefix reads it
+ * saves are large, so when the bound of those bytes, (num_members -
+ * num_groups) x max_prefix_len x num_kv_heads x head_dim x 4, is below
+ * 256 MiB per 64 members (at least 64) -- the crossover measured on GB300 --
+ * the call runs pa_decode (num_splits 0) on the same arguments instead, and
+ * the group description is not read.
  */
 int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
                       const int32_t* block_tables, const int32_t* context_lens,
@@ -323,7 +332,22 @@ int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v
                       pa_bf16* out, float* lse, const pa_shape* shape, void* workspace,
                       size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for pa_decode_cascade (0 if the arguments are invalid). */
+/* Policies of pa_decode_cascade_ex. */
+#define PA_CASCADE_AUTO 0   /* the cascade if its saved prefix bytes pay for it (see above) */
+#define PA_CASCADE_ALWAYS 1 /* always the cascade */
+#define PA_CASCADE_PLAIN 2  /* always plain pa_decode (the description is not read) */
+
+/* pa_decode_cascade with the choice made by the caller (policy, above). */
+int pa_decode_cascade_ex(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache,
+                         const int32_t* block_tables, const int32_t* context_lens,
+                         const int32_t* seq_group, int num_groups, const int32_t* cu_group,
+                         const int32_t* group_members, const int32_t* prefix_lens,
+                         int num_members, int max_group_size, int max_prefix_len, float scale,
+                         pa_bf16* out, float* lse, const pa_shape* shape, int policy,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for pa_decode_cascade and pa_decode_cascade_ex under any
+ * policy (0 if the arguments are invalid). */
 size_t pa_decode_cascade_workspace_size(const pa_shape* shape, int num_groups, int num_members,
                                         int max_group_size, int max_prefix_len);
 

@@ -45,6 +45,7 @@ EXPORTED = (
     "pa_decode_int8",
     "pa_decode_int8_workspace_size",
     "pa_decode_cascade",
+    "pa_decode_cascade_ex",
     "pa_decode_cascade_workspace_size",
     "pa_splitk_reduce",
     "pa_status_string",
@@ -113,6 +114,9 @@ def load(path: str | None = None):
         lib.pa_decode_cascade.restype = i32
         lib.pa_decode_cascade.argtypes = [V, V, V, V, V, V, i32, V, V, V, i32, i32, i32, f32,
                                           V, V, S, V, sz, V]
+        lib.pa_decode_cascade_ex.restype = i32
+        lib.pa_decode_cascade_ex.argtypes = [V, V, V, V, V, V, i32, V, V, V, i32, i32, i32, f32,
+                                             V, V, S, i32, V, sz, V]
         lib.pa_decode_cascade_workspace_size.restype = sz
         lib.pa_decode_cascade_workspace_size.argtypes = [S, i32, i32, i32, i32]
         lib.pa_splitk_reduce.restype = i32
@@ -255,11 +259,17 @@ def pa_decode_cascade_workspace_size(shape: pa_shape, num_groups: int, num_membe
                                                        int(max_prefix_len)))
 
 
+PA_CASCADE_AUTO = 0
+PA_CASCADE_ALWAYS = 1
+PA_CASCADE_PLAIN = 2
+
+
 def pa_decode_cascade(q, k_cache, v_cache, block_tables, context_lens, seq_group, cu_group,
                       group_members, prefix_lens, max_group_size, max_prefix_len, scale, out,
-                      lse=None, workspace=None, stream=None) -> None:
+                      lse=None, workspace=None, stream=None, policy=PA_CASCADE_AUTO) -> None:
     """Decode with shared prefixes attended once per group (same result as
-    pa_decode)."""
+    pa_decode). policy: PA_CASCADE_AUTO (the library decides whether the
+    cascade pays), PA_CASCADE_ALWAYS or PA_CASCADE_PLAIN."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -278,13 +288,15 @@ def pa_decode_cascade(q, k_cache, v_cache, block_tables, context_lens, seq_group
     if cu_group.shape[0] != G + 1 or seq_group.shape[0] != sh.num_seqs:
         raise ValueError("group description shapes do not match")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pa_decode_cascade(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                    _ptr(context_lens), _ptr(seq_group), G, _ptr(cu_group),
-                                    _ptr(group_members) if group_members.numel() else None,
-                                    _ptr(prefix_lens), int(group_members.numel()),
-                                    int(max_group_size), int(max_prefix_len), float(scale),
-                                    _ptr(out), _ptr(lse), ctypes.byref(sh), _ptr(workspace),
-                                    ws_bytes, _stream(stream)), "pa_decode_cascade")
+    _check(load().pa_decode_cascade_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), _ptr(context_lens), _ptr(seq_group),
+                                       G, _ptr(cu_group),
+                                       _ptr(group_members) if group_members.numel() else None,
+                                       _ptr(prefix_lens), int(group_members.numel()),
+                                       int(max_group_size), int(max_prefix_len), float(scale),
+                                       _ptr(out), _ptr(lse), ctypes.byref(sh), int(policy),
+                                       _ptr(workspace), ws_bytes, _stream(stream)),
+           "pa_decode_cascade")
 
 
 def pa_decode_int8_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:

@@ -87,8 +87,27 @@ int cascade_layout(const pa_shape* sh, int num_groups, int num_members, int max_
   L->dec_ws_bytes = S > 0 ? decode_rows_workspace_size(sh, L->suffix_sms) : 0;
   if (S > 0 && L->dec_ws_bytes == 0) return PA_ERR_ARG;
   L->dec_ws = take(L->dec_ws_bytes);
-  L->total = off;
+  // the plain balanced decode over the whole contexts uses the workspace
+  // from its start (policy PA_CASCADE_PLAIN, or PA_CASCADE_AUTO choosing it)
+  const size_t plain = S > 0 ? decode_rows_workspace_size(sh, 0) : 0;
+  L->total = off > plain ? off : plain;
   return PA_OK;
+}
+
+// Bytes of K/V rows the cascade saves at most: every member but the first of
+// a group skips reading the group's prefix, at most max_prefix_len tokens.
+// Measured on GB300 (shared-prompt batches of 16..128 sequences behind
+// prefixes of 256..4096 tokens, against pa_decode): the cascade is faster
+// once it saves about 256 MB per 64 members (its prefix tile and merge grow
+// with the members); below that its extra phases cost more than the prefix
+// reads they save, which plain decode mostly finds in L2.
+constexpr int64_t kCascadeMinSavedBytes = int64_t(256) << 20;
+
+bool cascade_pays(const pa_shape* sh, int num_groups, int num_members, int max_prefix_len) {
+  const int64_t per_token = (int64_t)sh->num_kv_heads * sh->head_dim * 2 * 2;
+  const int64_t saved = (int64_t)(num_members - num_groups) * max_prefix_len * per_token;
+  const int64_t scale = num_members > 64 ? num_members : 64;
+  return saved > 0 && saved * 64 >= kCascadeMinSavedBytes * scale;
 }
 
 // Everything the two halves need, in one grid-stride pass:
@@ -233,15 +252,18 @@ extern "C" size_t pa_decode_cascade_workspace_size(const pa_shape* shape, int nu
   return L.total;
 }
 
-extern "C" int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache,
-                                 const pa_bf16* v_cache, const int32_t* block_tables,
-                                 const int32_t* context_lens, const int32_t* seq_group,
-                                 int num_groups, const int32_t* cu_group,
-                                 const int32_t* group_members, const int32_t* prefix_lens,
-                                 int num_members, int max_group_size, int max_prefix_len,
-                                 float scale, pa_bf16* out, float* lse, const pa_shape* shape,
-                                 void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" int pa_decode_cascade_ex(const pa_bf16* q, const pa_bf16* k_cache,
+                                    const pa_bf16* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, const int32_t* seq_group,
+                                    int num_groups, const int32_t* cu_group,
+                                    const int32_t* group_members, const int32_t* prefix_lens,
+                                    int num_members, int max_group_size, int max_prefix_len,
+                                    float scale, pa_bf16* out, float* lse,
+                                    const pa_shape* shape, int policy, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
   pa::NvtxRange nvtx_range("pa_decode_cascade");
+  if (policy != PA_CASCADE_AUTO && policy != PA_CASCADE_ALWAYS && policy != PA_CASCADE_PLAIN)
+    return PA_ERR_ARG;
   int rc = check_shape_common(shape);
   if (rc != PA_OK) return rc;
   const int S = shape->num_seqs;
@@ -257,6 +279,11 @@ extern "C" int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache,
   if (rc != PA_OK) return rc;
   if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
     return PA_ERR_WORKSPACE;
+  if (policy == PA_CASCADE_PLAIN ||
+      (policy == PA_CASCADE_AUTO &&
+       !cascade_pays(shape, num_groups, num_members, max_prefix_len)))
+    return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse, shape, 0,
+                     workspace, workspace_bytes, stream);
   char* ws = static_cast<char*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   pa_bf16* q_g = reinterpret_cast<pa_bf16*>(ws + L.q_g);
@@ -310,4 +337,18 @@ extern "C" int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache,
     if (rc != PA_OK) return rc;
   }
   return pa_splitk_reduce(part_o, part_lse, S, Hq, 2, kHeadDim, out, lse, stream);
+}
+
+extern "C" int pa_decode_cascade(const pa_bf16* q, const pa_bf16* k_cache,
+                                 const pa_bf16* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, const int32_t* seq_group,
+                                 int num_groups, const int32_t* cu_group,
+                                 const int32_t* group_members, const int32_t* prefix_lens,
+                                 int num_members, int max_group_size, int max_prefix_len,
+                                 float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return pa_decode_cascade_ex(q, k_cache, v_cache, block_tables, context_lens, seq_group,
+                              num_groups, cu_group, group_members, prefix_lens, num_members,
+                              max_group_size, max_prefix_len, scale, out, lse, shape,
+                              PA_CASCADE_AUTO, workspace, workspace_bytes, stream);
 }

@@ -2,7 +2,8 @@
 reorganises the work -- shared prefix attended once per group, suffix per
 sequence, split-K merge -- so its reference is plain paged attention over
 each sequence's whole context: |out - ref| <= 1e-2 + 1e-2 |ref|,
-|lse - ref| <= 1e-3."""
+|lse - ref| <= 1e-3. The cases run the cascade's own phases (policy
+PA_CASCADE_ALWAYS); the last ones check which path the default policy takes."""
 import pytest
 import torch
 
@@ -21,7 +22,7 @@ def _lib():
     B.load()
 
 
-def cascade(db, groups=None, with_lse=True):
+def cascade(db, groups=None, with_lse=True, policy=B.PA_CASCADE_ALWAYS):
     w, dev = db.w, db.dev
     sg, cu, mem, pl, mg, mp = W.cascade_groups(w) if groups is None else groups
     sg, cu, mem, pl = sg.to(dev), cu.to(dev), mem.to(dev), pl.to(dev)
@@ -31,7 +32,7 @@ def cascade(db, groups=None, with_lse=True):
     ws = B.workspace(B.pa_decode_cascade_workspace_size(sh, pl.shape[0], mem.numel(), mg, mp),
                      dev)
     B.pa_decode_cascade(db.q, db.kc, db.vc, db.block_tables, db.context_lens, sg, cu, mem, pl,
-                        mg, mp, w.scale, out, lse, workspace=ws)
+                        mg, mp, w.scale, out, lse, workspace=ws, policy=policy)
     return out, lse
 
 
@@ -124,3 +125,30 @@ def test_cascade_shared_prompt_matches_oracle(sizes):
     assert B.pa_debug_read_error() == 0
     ref, ref_lse = oracle_attention(w)
     assert_attention_close(out, lse, ref, ref_lse, what=f"cascade shared prompt {sizes}")
+
+
+def test_auto_policy_takes_plain_decode_when_the_prefix_is_short():
+    # ragged batch: 77 sequences behind a 512-token prefix save at most
+    # 76 x 512 x 4 KB = 159 MB of prefix reads, below 256 MiB x 77/64: the
+    # default policy runs pa_decode itself (the same bits)
+    w = W.ragged(seed=37)
+    db = DeviceBatch(w)
+    out, lse = cascade(db, policy=B.PA_CASCADE_AUTO)
+    ref_out, ref_lse = db.decode(0)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse, ref_lse)
+
+
+def test_auto_policy_takes_the_cascade_behind_a_long_prompt():
+    # 128 sequences behind a 4096-token prompt save about 2.1 GB: the default
+    # policy runs the cascade (the same bits as forcing it)
+    w = W.shared_prompt(seed=38)
+    db = DeviceBatch(w)
+    out, lse = cascade(db, policy=B.PA_CASCADE_AUTO)
+    out2, lse2 = cascade(db, policy=B.PA_CASCADE_ALWAYS)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2)
