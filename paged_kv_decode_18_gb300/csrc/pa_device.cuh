@@ -400,6 +400,84 @@ __device__ __forceinline__ int range_start(int w, int W, int nw) {
   return (int)(((long long)w * W) / nw);
 }
 
+// The equal cut as an object: worker w starts at range_start(w); tile x is held
+// by worker floor(((x + 1) * nw - 1) / W).
+struct EqualCut {
+  int W, nw;
+  __device__ __forceinline__ int start(int w) const { return range_start(w, W, nw); }
+  __device__ __forceinline__ int owner(int x) const {
+    return (int)(((long long)(x + 1) * nw - 1) / W);
+  }
+};
+
+// A cut that charges every segment start `cost4`/4 of a tile on top of the
+// tiles themselves (starting a segment costs its query tile, a first score
+// tile with nothing to overlap, and a write-out), so a worker whose range
+// holds many short segments gets fewer tiles. The cost of tiles 0 .. x-1 is
+// 4x + cost4 * (segment starts below x); worker w starts at the first x whose
+// cost reaches floor(w * C / nw), C the total. The starts live in a shared
+// array of nw + 1 entries, built by build_piece_cut.
+struct PieceCut {
+  const int* cut;  // [nw + 1] first tile of each worker; cut[nw] = total
+  int nw;
+  __device__ __forceinline__ int start(int w) const { return cut[w]; }
+  // largest w with cut[w] <= x: the worker holding tile x
+  __device__ __forceinline__ int owner(int x) const { return upper_index(cut, 0, nw, x); }
+};
+
+// Build the PieceCut of a plan into cut[0 .. nw] (nw + 1 <= max_workers + 1
+// ints). All threads of the CTA call it; it ends with a CTA barrier. Needs
+// every pair to hold at least one tile per KV head (true of every query-tile
+// plan), so pair p begins after p * Hkv segment starts: its tiles cost
+// base(p) = 4 pair_off[p] + cost4 p Hkv before it. One thread per worker finds
+// the pair its target falls in by bisection, then the tile in closed form.
+// With nw <= C / (4 + cost4), consecutive targets are at least one tile's
+// largest cost apart, so the starts strictly increase: no worker is empty.
+__device__ inline PieceCut build_piece_cut(const PlanSmem& P, int Hkv, int max_workers, int cost4,
+                                           int* cut) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const long long C = 4LL * P.total + (long long)cost4 * P.npairs * Hkv;
+  long long nwl = C / (4 + cost4);
+  if (nwl > max_workers) nwl = max_workers;
+  if (nwl < 1) nwl = 1;
+  const int nw = (int)nwl;
+  const bool narrow = C * nw < (1LL << 32);  // targets in 32-bit arithmetic
+  auto base = [&](int p) -> long long {
+    return 4LL * P.pair_off[p] + (long long)cost4 * p * Hkv;
+  };
+  for (int w = 1 + tid; w < nw; w += nthreads) {
+    const long long T = narrow ? (long long)((uint32_t)w * (uint32_t)C / (uint32_t)nw)
+                               : ((long long)w * C) / nw;  // 0 < T < C
+    // the pair p with base(p) < T <= base(p + 1)
+    int lo = 0, hi = P.npairs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (base(mid) < T)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int o0 = P.pair_off[lo];
+    const int nt = (P.pair_off[lo + 1] - o0) / Hkv;
+    const int D = (int)(T - base(lo));  // 1 .. Hkv (4 nt + cost4)
+    const int seg = 4 * nt + cost4;     // cost of one whole segment of this pair
+    const int h = (D - 1) / seg;        // the segment it falls in
+    const int rem = D - h * seg;        // 1 .. seg
+    // tile r (1-based) of segment h costs cost4 + 4r up to and including it
+    const int r = max(1, (rem - cost4 + 3) / 4);
+    cut[w] = o0 + h * nt + r;
+  }
+  if (tid == 0) {
+    cut[0] = 0;
+    cut[nw] = P.total;
+  }
+  __syncthreads();
+  PieceCut c;
+  c.cut = cut;
+  c.nw = nw;
+  return c;
+}
+
 // The merge a worker boundary owns. A segment (pair, kv head) cut by range
 // boundaries is merged by the first boundary inside it: boundary w owns the
 // segment containing tile range_start(w) when that segment began inside worker
@@ -411,22 +489,29 @@ struct MergeJob {
   int s, qt, h, last, slot_prev;
 };
 
-__device__ inline MergeJob merge_job(const PlanSmem& P, int S, int Hkv, int w, int W, int nw) {
+template <class Cut>
+__device__ inline MergeJob merge_job_of(const PlanSmem& P, int S, int Hkv, int w, int nw,
+                                        const Cut& cut) {
   MergeJob j;
   j.valid = false;
   if (w <= 0 || w >= nw) return j;
-  const int R0 = range_start(w, W, nw);
+  const int R0 = cut.start(w);
+  if (R0 >= P.total) return j;
   const TilePos t = locate(P, S, Hkv, R0);
   const int A = R0 - t.b;  // flat start of the segment
-  const int R0prev = range_start(w - 1, W, nw);
+  const int R0prev = cut.start(w - 1);
   if (t.b == 0 || A < R0prev) return j;
   j.valid = true;
   j.s = t.s;
   j.qt = t.qt;
   j.h = t.h;
-  j.last = (int)(((long long)(A + t.nt) * nw - 1) / W);  // worker holding the last tile
+  j.last = cut.owner(A + t.nt - 1);  // worker holding the last tile
   j.slot_prev = (A == R0prev) ? 0 : 1;
   return j;
+}
+
+__device__ inline MergeJob merge_job(const PlanSmem& P, int S, int Hkv, int w, int W, int nw) {
+  return merge_job_of(P, S, Hkv, w, nw, EqualCut{W, nw});
 }
 
 // Step a position to the next flat tile (only called while idx + 1 < total).

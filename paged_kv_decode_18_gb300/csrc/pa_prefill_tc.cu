@@ -55,6 +55,10 @@ constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffLx = kOffBar + 256;       // [2 pieces][2 halves][128 rows] x (m, l)
 constexpr int kOffPlan = kOffLx + 2 * 2 * kRowsT * 8;
+// a segment start weighs as much as one key tile in the cut between CTAs
+// (measured: a CTA whose range starts many short segments spends about one
+// tile's time more on each)
+constexpr int kPieceCost4 = 4;
 constexpr int kSoftmaxWarps = 8;            // warps 2-9, two per SM sub-partition
 constexpr int kVWarp = 2 + kSoftmaxWarps;   // the V producer
 constexpr int kThreadsT = 96 + kSoftmaxWarps * 32;
@@ -252,6 +256,11 @@ __device__ __forceinline__ void plan_view(unsigned char* base, const TcArgs& a, 
   P.qstart = P.ctx + a.S;
 }
 
+// The worker starts of the piece-weighted cut, after the plan arrays.
+__device__ __forceinline__ int* cut_view(unsigned char* base, const TcArgs& a) {
+  return reinterpret_cast<int*>(base) + (a.npairs_cap + 1) + 3 * (a.S + 1);
+}
+
 __global__ void __launch_bounds__(kThreadsT, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                             const __grid_constant__ CUtensorMap tmk,
@@ -286,13 +295,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   PlanInputs in;
   plan_inputs(a, in);
   build_plan(in, P, nullptr);  // ends with a CTA barrier
+  const PieceCut cut = build_piece_cut(P, Hkv, a.num_workers, kPieceCost4, cut_view(smem + kOffPlan, a));
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const int W = P.total;
-  const int nw = min(a.num_workers, W);
   const int w = blockIdx.x;
-  if (w >= nw) return;  // the whole CTA is idle (uniform)
-  const int R0 = range_start(w, W, nw), R1 = range_start(w + 1, W, nw);
+  if (w >= cut.nw) return;  // the whole CTA is idle (uniform)
+  const int R0 = cut.start(w), R1 = cut.start(w + 1);
   if (R0 >= R1) return;
 
   if (warp == 1) {
@@ -697,10 +705,9 @@ __global__ void __launch_bounds__(kFixThreads)
   PlanInputs in;
   plan_inputs(a, in);
   build_plan(in, P, nullptr);
-  const int W = P.total;
-  const int nw = min(a.num_workers, W);
+  const PieceCut cut = build_piece_cut(P, a.Hkv, a.num_workers, kPieceCost4, cut_view(fx_smem, a));
   const int w = blockIdx.x;
-  const MergeJob job = merge_job(P, a.S, a.Hkv, w, W, nw);
+  const MergeJob job = merge_job_of(P, a.S, a.Hkv, w, cut.nw, cut);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!job.valid) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -791,8 +798,9 @@ bool make_q_map(CUtensorMap* map, const void* q, int64_t num_q_tokens, int Hq, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t plan_bytes(int S, int npairs_cap) {
-  return sizeof(int) * ((size_t)npairs_cap + 1 + 3 * (size_t)S + 2);
+// plan arrays, then the worker starts of the cut
+size_t plan_bytes(int S, int npairs_cap, int workers) {
+  return sizeof(int) * ((size_t)npairs_cap + 1 + 3 * ((size_t)S + 1) + (size_t)workers + 1);
 }
 
 }  // namespace
@@ -815,8 +823,11 @@ int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
   g->enabled = true;
   g->npairs_cap = (int)(cap < 1 ? 1 : cap);
   g->QTb = QTb;
-  g->smem = 1024 + kOffPlan + round_up(plan_bytes(S, g->npairs_cap), 16);
-  g->fixup_smem = plan_bytes(S, g->npairs_cap);
+  // one CTA per SM (shared memory and TMEM limit it to one)
+  g->grid = max_ctas > 0 && max_ctas < dev.num_sms ? max_ctas : dev.num_sms;
+  g->workers = g->grid;
+  g->smem = 1024 + kOffPlan + round_up(plan_bytes(S, g->npairs_cap, g->workers), 16);
+  g->fixup_smem = plan_bytes(S, g->npairs_cap, g->workers);
   if (g->smem > (size_t)dev.max_smem_optin || g->fixup_smem > (size_t)dev.max_smem_optin)
     return PA_ERR_UNSUPPORTED;
   if (!raise_smem_limit(reinterpret_cast<const void*>(paged_prefill_tc_kernel)))
@@ -824,9 +835,6 @@ int prefill_tc_geometry(const pa_shape* sh, int64_t num_q_tokens, int max_q_len,
   if (g->fixup_smem > 48 * 1024 &&
       !raise_smem_limit(reinterpret_cast<const void*>(prefill_tc_fixup_kernel)))
     return PA_ERR_CUDA;
-  // one CTA per SM (shared memory and TMEM limit it to one)
-  g->grid = max_ctas > 0 && max_ctas < dev.num_sms ? max_ctas : dev.num_sms;
-  g->workers = g->grid;
   g->ws_lse = round_up(sizeof(float) * 2 * kRowsT * (size_t)g->workers, 256);
   g->ws_o = round_up(sizeof(float) * 2 * kRowsT * kHeadDim * (size_t)g->workers, 256);
   g->ws_bytes = g->ws_lse + g->ws_o;
