@@ -552,18 +552,19 @@ def run_secondary_varlen(w, dev, B, peak):
 
 def run_secondary_int8(ws_by_name, dev, B, peak):
     """Decode over the INT8 pool (quantised cache write, fused dequant): the
-    engine batch rotated over the layer pools, the ragged and the long batch."""
+    engine and ragged batches rotated over the layer pools (as their bf16
+    lines are), and the long batch (one pool, larger than L2)."""
     res = {}
-    for name, nlayers in (("engine", LAYERS), ("ragged", 1), ("long", 1)):
+    for name, nlayers in (("engine", LAYERS), ("ragged", LAYERS), ("long", 1)):
         w = ws_by_name[name]
         pools = []
         kh, vh, sh_ = w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev)
         kn, vn, sn = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
         for _ in range(nlayers):
-            kc, vc, ks, vs = w.empty_pool_i8(dev)
-            B.pa_reshape_and_cache_int8(kh, vh, sh_, kc, vc, ks, vs)
-            B.pa_reshape_and_cache_int8(kn, vn, sn, kc, vc, ks, vs)
-            pools.append((kc, vc, ks, vs))
+            kc, vc = w.empty_pool_i8(dev)
+            B.pa_reshape_and_cache_int8(kh, vh, sh_, kc, vc)
+            B.pa_reshape_and_cache_int8(kn, vn, sn, kc, vc)
+            pools.append((kc, vc))
         del kh, vh, sh_
         q = w.q.to(dev)
         bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
@@ -574,9 +575,9 @@ def run_secondary_int8(ws_by_name, dev, B, peak):
         ctr = [0]
 
         def call():
-            kc, vc, ks, vs = pools[ctr[0] % nlayers]
+            kc, vc = pools[ctr[0] % nlayers]
             ctr[0] += 1
-            B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse, num_splits=0,
+            B.pa_decode_int8(q, kc, vc, bt, cl, w.scale, out, lse, num_splits=0,
                              workspace=ws)
         ms = time_graph_calls(call, per_replay=4 if nlayers > 1 else 2)
         alg = decode_algorithmic_bytes(w, unique=True, kv_bytes_per_token=int8_bytes_per_token(w))
@@ -585,7 +586,7 @@ def run_secondary_int8(ws_by_name, dev, B, peak):
                                "achieved_gbs": round(gbs, 1),
                                "frac_of_measured_peak": round(gbs / peak, 4),
                                "value": w.num_q_tokens / (ms / 1e3), "unit": UNIT,
-                               "kv_format": "int8 + fp32 row scales"}
+                               "kv_format": "int8 codes + fp32 row scales, one 2112-byte tile"}
         del pools
         torch.cuda.empty_cache()
     return res
@@ -760,9 +761,9 @@ def run_case(args, dev):
         w = W.make(args.case, seed=args.seed)
     int8 = args.case.endswith("_int8")
     if int8:
-        kc, vc, ks, vs = w.empty_pool_i8(dev)
+        kc, vc = w.empty_pool_i8(dev)
         B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                    kc, vc, ks, vs)
+                                    kc, vc)
     else:
         kc, vc = w.empty_pool(dev)
         B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
@@ -788,8 +789,8 @@ def run_case(args, dev):
 
     def step():
         if int8:
-            B.pa_reshape_and_cache_int8(k_new, v_new, slot_new, kc, vc, ks, vs)
-            B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse,
+            B.pa_reshape_and_cache_int8(k_new, v_new, slot_new, kc, vc)
+            B.pa_decode_int8(q, kc, vc, bt, cl, w.scale, out, lse,
                              num_splits=args.splits, workspace=ws)
             return
         B.pa_reshape_and_cache(k_new, v_new, slot_new, kc, vc)

@@ -241,10 +241,12 @@ size_t pa_decode_varlen_workspace_size(const pa_shape* shape, int64_t num_q_toke
  * outliers in check and dequantisation must be fused or it moves more bytes
  * than fp16). A second pool format that halves the bytes of the decode stream:
  *
- *   k_cache, v_cache  int8, [num_blocks][num_kv_heads][block_size][head_dim]
- *                     (2 KB per (block, KV head) tile)
- *   k_scale, v_scale  fp32, [num_blocks][num_kv_heads][block_size]: one
- *                     scale per (token, KV head) row of head_dim values
+ *   k_cache, v_cache  bytes, [num_blocks][num_kv_heads][PA_INT8_TILE_BYTES]:
+ *                     one tile per (block, KV head) = the block_size rows'
+ *                     codes, int8 [block_size][head_dim] (2048 bytes), then
+ *                     the same rows' fp32 scales [block_size] (64 bytes); one
+ *                     scale per (token, KV head) row of head_dim values.
+ *                     A tile is one contiguous 2112-byte run (a multiple of 16).
  *
  * Row quantisation (symmetric, group = one head row): amax = max_d |x_d|;
  * if amax == 0 every code is 0 and the scale 0; otherwise
@@ -254,33 +256,34 @@ size_t pa_decode_varlen_workspace_size(const pa_shape* shape, int64_t num_q_toke
  * code_d * scale. Rows are written once, so a block's earlier rows never
  * change when later tokens arrive.
  */
+#define PA_INT8_TILE_BYTES 2112
 
 /*
  * pa_reshape_and_cache_int8 -- pa_reshape_and_cache into the int8 pool: for
  * every t with slot_mapping[t] >= 0, row k[t][h][:] is quantised as above
- * into k_cache[slot / BS][h][slot % BS][:] and k_scale[slot / BS][h][slot % BS]
- * (V alike). Pointers 16-byte aligned (slot_mapping 8). Same slot rules and
- * error bits as pa_reshape_and_cache. bf16 inputs that are subnormal are
- * read as zero (the kernels flush fp32 subnormals).
+ * into the codes of row slot % BS of tile (slot / BS, h) of k_cache and its
+ * scale into that tile's scale slot slot % BS (V alike). Pointers 16-byte
+ * aligned (slot_mapping 8). Same slot rules and error bits as
+ * pa_reshape_and_cache. bf16 inputs that are subnormal are read as zero (the
+ * kernels flush fp32 subnormals).
  */
 int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v, const int64_t* slot_mapping,
-                              int64_t num_tokens, int8_t* k_cache, int8_t* v_cache,
-                              float* k_scale, float* v_scale, const pa_shape* shape,
-                              void* stream);
+                              int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                              const pa_shape* shape, void* stream);
 
 /*
  * pa_decode_int8 -- pa_decode over the int8 pool, dequantisation fused: each
  * score is the int8 row dot product times the row's K scale, and each
  * softmax weight is multiplied by the row's V scale before it meets the
  * int8 V row. Same arguments, splits, outputs and workspace rules as
- * pa_decode (workspace from pa_decode_int8_workspace_size). The result is
- * attention over the dequantised rows, within fp32 rounding.
+ * pa_decode (workspace from pa_decode_int8_workspace_size); k_cache and
+ * v_cache 16-byte aligned. The result is attention over the dequantised
+ * rows, within fp32 rounding.
  */
-int pa_decode_int8(const pa_bf16* q, const int8_t* k_cache, const int8_t* v_cache,
-                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                   const int32_t* context_lens, float scale, pa_bf16* out, float* lse,
-                   const pa_shape* shape, int num_splits, void* workspace,
-                   size_t workspace_bytes, void* stream);
+int pa_decode_int8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens, float scale,
+                   pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes for pa_decode_int8 with this shape and split choice. */
 size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_splits);

@@ -106,9 +106,9 @@ def load(path: str | None = None):
         lib.pa_decode_varlen_workspace_size.restype = sz
         lib.pa_decode_varlen_workspace_size.argtypes = [S, i64, i32]
         lib.pa_reshape_and_cache_int8.restype = i32
-        lib.pa_reshape_and_cache_int8.argtypes = [V, V, V, i64, V, V, V, V, S, V]
+        lib.pa_reshape_and_cache_int8.argtypes = [V, V, V, i64, V, V, S, V]
         lib.pa_decode_int8.restype = i32
-        lib.pa_decode_int8.argtypes = [V, V, V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
+        lib.pa_decode_int8.argtypes = [V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
         lib.pa_decode_int8_workspace_size.restype = sz
         lib.pa_decode_int8_workspace_size.argtypes = [S, i32]
         lib.pa_decode_cascade.restype = i32
@@ -172,10 +172,23 @@ def make_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_bl
                     int(block_size), int(max_blocks_per_seq), int(num_blocks))
 
 
+# bytes of one (block, KV head) tile of the int8 pool: 16 x 128 codes, then
+# the 16 rows' fp32 scales
+PA_INT8_TILE_BYTES = 2112
+INT8_BLOCK, INT8_HEAD_DIM = 16, 128
+
+
 def shape_of(q, k_cache, block_tables, num_seqs=None) -> pa_shape:
-    """Shape struct from the tensors: q [*, Hq, D], k_cache [NB, Hkv, BS, D],
+    """Shape struct from the tensors: q [*, Hq, D], k_cache [NB, Hkv, BS, D]
+    (bf16) or [NB, Hkv, PA_INT8_TILE_BYTES] (uint8, the int8 pool),
     block_tables [S, max_blocks]."""
-    NB, Hkv, BS, D = k_cache.shape
+    if k_cache.dim() == 3 and k_cache.dtype == torch.uint8:
+        if k_cache.shape[2] != PA_INT8_TILE_BYTES:
+            raise ValueError(f"int8 pool tiles must be {PA_INT8_TILE_BYTES} bytes")
+        NB, Hkv = k_cache.shape[:2]
+        BS, D = INT8_BLOCK, INT8_HEAD_DIM
+    else:
+        NB, Hkv, BS, D = k_cache.shape
     S = block_tables.shape[0] if num_seqs is None else num_seqs
     return make_shape(S, q.shape[1], Hkv, D, BS, block_tables.shape[1], NB)
 
@@ -228,27 +241,24 @@ def pa_decode_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
     return int(load().pa_decode_workspace_size(ctypes.byref(shape), int(num_splits)))
 
 
-def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
-                              stream=None) -> None:
-    """Quantising cache write into the int8 pool (one fp32 scale per row)."""
+def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Quantising cache write into the int8 pool (uint8 tiles [NB, Hkv, 2112]:
+    a tile's 16 x 128 codes, then its 16 fp32 row scales)."""
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
     _need(slot_mapping, "slot_mapping", torch.int64, 1)
-    _need(k_cache, "k_cache", torch.int8, 4)
-    _need(v_cache, "v_cache", torch.int8, 4)
-    _need(k_scale, "k_scale", torch.float32, 3)
-    _need(v_scale, "v_scale", torch.float32, 3)
-    if k.shape != v.shape or k_cache.shape != v_cache.shape or k_scale.shape != v_scale.shape:
-        raise ValueError("k/v, cache or scale shapes differ")
+    _need(k_cache, "k_cache", torch.uint8, 3)
+    _need(v_cache, "v_cache", torch.uint8, 3)
+    if k.shape != v.shape or k_cache.shape != v_cache.shape:
+        raise ValueError("k/v or cache shapes differ")
     if slot_mapping.shape[0] != k.shape[0]:
         raise ValueError("slot_mapping length != number of tokens")
-    NB, Hkv, BS, D = k_cache.shape
-    if k.shape[1:] != (Hkv, D) or k_scale.shape != (NB, Hkv, BS):
-        raise ValueError("k rows or scales do not match the cache")
-    sh = make_shape(0, Hkv, Hkv, D, BS, 0, NB)
+    sh = shape_of(k, k_cache, torch.empty((0, 0)))
+    if k.shape[1:] != (sh.num_kv_heads, sh.head_dim):
+        raise ValueError("k rows do not match the cache")
     _check(load().pa_reshape_and_cache_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
-                                            _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                            _ptr(v_scale), ctypes.byref(sh), _stream(stream)),
+                                            _ptr(k_cache), _ptr(v_cache), ctypes.byref(sh),
+                                            _stream(stream)),
            "pa_reshape_and_cache_int8")
 
 
@@ -303,32 +313,29 @@ def pa_decode_int8_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
     return int(load().pa_decode_int8_workspace_size(ctypes.byref(shape), int(num_splits)))
 
 
-def pa_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
-                   out, lse=None, num_splits: int = 0, workspace=None, stream=None) -> None:
+def pa_decode_int8(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
+                   num_splits: int = 0, workspace=None, stream=None) -> None:
     """Decode over the int8 pool with the dequantisation fused."""
     _need(q, "q", torch.bfloat16, 3)
-    _need(k_cache, "k_cache", torch.int8, 4)
-    _need(v_cache, "v_cache", torch.int8, 4)
-    _need(k_scale, "k_scale", torch.float32, 3)
-    _need(v_scale, "v_scale", torch.float32, 3)
+    _need(k_cache, "k_cache", torch.uint8, 3)
+    _need(v_cache, "v_cache", torch.uint8, 3)
     _need(block_tables, "block_tables", torch.int32, 2)
     _need(context_lens, "context_lens", torch.int32, 1)
     _need(out, "out", torch.bfloat16, 3)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
-    if k_cache.shape != v_cache.shape or k_scale.shape != k_cache.shape[:3] or \
-            v_scale.shape != k_scale.shape:
-        raise ValueError("cache / scale shapes differ")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k / v cache shapes differ")
     sh = shape_of(q, k_cache, block_tables)
     if q.shape[0] != sh.num_seqs or context_lens.shape[0] != sh.num_seqs:
         raise ValueError("q / context_lens rows != number of sequences")
     if out.shape != q.shape:
         raise ValueError("out shape != q shape")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pa_decode_int8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                 _ptr(v_scale), _ptr(block_tables), _ptr(context_lens),
-                                 float(scale), _ptr(out), _ptr(lse), ctypes.byref(sh),
-                                 int(num_splits), _ptr(workspace), ws_bytes, _stream(stream)),
+    _check(load().pa_decode_int8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                 _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
+                                 ctypes.byref(sh), int(num_splits), _ptr(workspace), ws_bytes,
+                                 _stream(stream)),
            "pa_decode_int8")
 
 

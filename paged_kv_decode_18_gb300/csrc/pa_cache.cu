@@ -49,7 +49,7 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
 // scale = 0. Division and product are IEEE-rounded fp32 operations (explicit
 // _rn intrinsics, no contraction), rint rounds half to even. The row lands
 // as 128 contiguous bytes of the (block, KV head) int8 tile and one float of
-// the [num_blocks][Hkv][16] scale array.
+// the same tile's scale slots.
 __device__ __forceinline__ void quantize_row_to(const uint2 x, int lane, int8_t* __restrict__ dst,
                                                 float* __restrict__ scale_dst) {
   const float f0 = bf_lo(x.x), f1 = bf_hi(x.x), f2 = bf_lo(x.y), f3 = bf_hi(x.y);
@@ -74,10 +74,8 @@ __global__ void reshape_and_cache_int8_kernel(const uint2* __restrict__ k,
                                               const uint2* __restrict__ v,
                                               const int64_t* __restrict__ slots, int64_t rows,
                                               int Hkv, int64_t num_slots,
-                                              int8_t* __restrict__ k_cache,
-                                              int8_t* __restrict__ v_cache,
-                                              float* __restrict__ k_scale,
-                                              float* __restrict__ v_scale) {
+                                              uint8_t* __restrict__ k_cache,
+                                              uint8_t* __restrict__ v_cache) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -92,11 +90,14 @@ __global__ void reshape_and_cache_int8_kernel(const uint2* __restrict__ k,
     return;
   }
   const int64_t blk = slot / kBlock, off = slot % kBlock;
-  const int64_t dst_row = (blk * Hkv + h) * kBlock + off;  // row index in [NB][Hkv][16]
+  // tile (blk, h): 16 rows of 128 codes, then the 16 rows' fp32 scales
+  const int64_t tile = (blk * Hkv + h) * kInt8TileBytes;
   // lane reads dims 4*lane .. 4*lane+3 (8 bytes): the warp reads the 256-byte row
   const uint2 xk = k[row * 32 + lane], xv = v[row * 32 + lane];
-  quantize_row_to(xk, lane, k_cache + dst_row * kHeadDim, k_scale + dst_row);
-  quantize_row_to(xv, lane, v_cache + dst_row * kHeadDim, v_scale + dst_row);
+  quantize_row_to(xk, lane, reinterpret_cast<int8_t*>(k_cache + tile) + off * kHeadDim,
+                  reinterpret_cast<float*>(k_cache + tile + kBlock * kHeadDim) + off);
+  quantize_row_to(xv, lane, reinterpret_cast<int8_t*>(v_cache + tile) + off * kHeadDim,
+                  reinterpret_cast<float*>(v_cache + tile + kBlock * kHeadDim) + off);
 }
 
 }  // namespace
@@ -151,17 +152,16 @@ extern "C" int pa_reshape_and_cache(const pa_bf16* k, const pa_bf16* v,
 
 extern "C" int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v,
                                          const int64_t* slot_mapping, int64_t num_tokens,
-                                         int8_t* k_cache, int8_t* v_cache, float* k_scale,
-                                         float* v_scale, const pa_shape* shape, void* stream) {
+                                         uint8_t* k_cache, uint8_t* v_cache,
+                                         const pa_shape* shape, void* stream) {
   pa::NvtxRange nvtx_range("pa_reshape_and_cache_int8");
   int rc = check_shape_common(shape);
   if (rc != PA_OK) return rc;
   if (num_tokens < 0) return PA_ERR_ARG;
   if (num_tokens == 0) return PA_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
-    return PA_ERR_ARG;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(k_scale, 16) || !aligned(v_scale, 16) || !aligned(slot_mapping, 8))
+      !aligned(slot_mapping, 8))
     return PA_ERR_ARG;
   const int64_t rows = num_tokens * shape->num_kv_heads;
   const int wpb = 8;
@@ -171,7 +171,7 @@ extern "C" int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v,
                        static_cast<cudaStream_t>(stream), reinterpret_cast<const uint2*>(k),
                        reinterpret_cast<const uint2*>(v), slot_mapping, rows,
                        shape->num_kv_heads, shape->num_blocks * shape->block_size, k_cache,
-                       v_cache, k_scale, v_scale) != cudaSuccess)
+                       v_cache) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }

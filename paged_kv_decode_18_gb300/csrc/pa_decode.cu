@@ -43,15 +43,19 @@ namespace {
 constexpr int kG = 2;                          // query heads per KV head (built)
 constexpr int kQBytes = kG * kHeadDim * 2;     // 512
 
-// Stage layout for a KV element format: bf16 tiles (4 KB each), or int8
-// tiles (2 KB each) followed by the tile's 16 K scales and 16 V scales.
+// Stage layout for a KV element format: the K tile, the V tile, then q (at a
+// piece's first tile). A tile is one bulk copy of the pool's (block, KV head)
+// run: bf16 [16][128] (4 KB), or int8 codes [16][128] (2 KB) followed by the
+// 16 rows' fp32 scales.
 template <bool Q8>
 struct KvFormat {
-  static constexpr int kTile = Q8 ? kBlock * kHeadDim : kTileBytes;  // one K or V tile, bytes
-  static constexpr int kRow = kTile / kBlock;                        // one token row, bytes
-  static constexpr int kScaleOff = 2 * kTile;
-  static constexpr int kQOff = kScaleOff + (Q8 ? 2 * kBlock * 4 : 0);
+  static constexpr int kTile = Q8 ? kInt8TileBytes : kTileBytes;  // one K or V tile, bytes
+  static constexpr int kRow = Q8 ? kHeadDim : 2 * kHeadDim;      // one token row's values, bytes
+  static constexpr int kScaleOff = kBlock * kHeadDim;            // int8: scales within a tile
+  static constexpr int kQOff = 2 * kTile;
   static constexpr int kStage = kQOff + kQBytes;
+  static_assert(kTile % 16 == 0 && kStage % 16 == 0, "bulk copies need 16-byte alignment");
+  static_assert(!Q8 || kScaleOff + kBlock * 4 == kTile, "int8 scales end the tile");
 };
 
 template <int NSTAGE, bool Q8>
@@ -66,10 +70,8 @@ enum : int { kBalanced = 0, kFixed = 1 };
 
 struct DecodeArgs {
   const uint16_t* q;
-  const unsigned char* k_cache;  // bf16 or int8 tiles
+  const unsigned char* k_cache;  // bf16 or int8 tiles (KvFormat)
   const unsigned char* v_cache;
-  const float* k_scale;          // int8: [num_blocks][Hkv][16] per-row scales
-  const float* v_scale;
   const int32_t* block_tables;
   const int32_t* context_lens;
   uint16_t* out;
@@ -406,11 +408,6 @@ __global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
       const size_t tile = (size_t)phys * Hkv + pp.h;
       bulk_copy_g2s(smem_addr(st), a.k_cache + tile * F::kTile, F::kTile, bar);
       bulk_copy_g2s(smem_addr(st + F::kTile), a.v_cache + tile * F::kTile, F::kTile, bar);
-      if constexpr (Q8) {
-        bulk_copy_g2s(smem_addr(st + F::kScaleOff), a.k_scale + tile * kBlock, kBlock * 4, bar);
-        bulk_copy_g2s(smem_addr(st + F::kScaleOff + kBlock * 4), a.v_scale + tile * kBlock,
-                      kBlock * 4, bar);
-      }
       if (first)
         bulk_copy_g2s(smem_addr(st + F::kQOff),
                       a.q + ((size_t)pp.s * Hq + (size_t)pp.h * kG) * kHeadDim, kQBytes, bar);
@@ -544,7 +541,8 @@ __global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
         // replaced by 0. The row's V scale folds into its weights.
         float2 vf[8];
         load_row16<Q8>(Vs + i * F::kRow, vf);
-        const float vs = reinterpret_cast<const float*>(st + F::kScaleOff + kBlock * 4)[grp * 4 + i];
+        const float vs =
+            reinterpret_cast<const float*>(st + F::kTile + F::kScaleOff)[grp * 4 + i];
         const float vsc = grp * 4 + i < nvalid ? vs : 0.f;
         const float2 p0 = make_float2(pv[2 * i] * vsc, pv[2 * i] * vsc);
         const float2 p1 = make_float2(pv[2 * i + 1] * vsc, pv[2 * i + 1] * vsc);
@@ -849,11 +847,11 @@ constexpr int kWarps = 6;
 // (engine, ragged) run best with 6 warps x 2 CTAs per SM.
 constexpr int kWarpsLong = 8;
 constexpr int kStages = 2;    // bf16: 2 x 8 KB of copies in flight per warp
-// int8: 8 warps x 2 stages of 4 KB, two CTAs per SM (16 warps at 128
-// registers). The int8 loop is bound by instruction issue (the dequantising
-// conversions), not by copies in flight, so it takes more warps rather than
-// more stages: measured 3-5% faster than 6 warps x 3 stages.
-constexpr int kWarpsQ8 = 8;
+// int8: 6 warps x 2 stages of 4.6 KB (a K and a V tile, each one copy of
+// codes and scales), two CTAs per SM. The int8 loop is bound by instruction
+// issue (the dequantising conversions), not by copies in flight: a sweep of
+// 4-8 warps x 2-3 stages put this shape level with the best on every batch.
+constexpr int kWarpsQ8 = 6;
 constexpr int kStagesQ8 = 2;
 
 struct DecodeGeometry;
@@ -1008,23 +1006,19 @@ thread_local int g_inject_missing_copy = -1;
 
 // Validate, size and launch the decode grid and its merge. `early`: see the
 // kernel (only pa_append_decode sets it).
-// k_scale / v_scale non-null selects the int8 format.
-int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
-                const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                const int32_t* context_lens, float scale, pa_bf16* out, float* lse,
-                const pa_shape* shape, int num_splits, void* workspace, size_t workspace_bytes,
-                cudaStream_t st, int early, const RowsOut* rows = nullptr, int late = 0,
-                int max_sms = 0) {
-  const bool q8 = k_scale != nullptr;
+// q8 selects the int8 pool format.
+int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache, bool q8,
+                const int32_t* block_tables, const int32_t* context_lens, float scale,
+                pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+                void* workspace, size_t workspace_bytes, cudaStream_t st, int early,
+                const RowsOut* rows = nullptr, int late = 0, int max_sms = 0) {
   int rc = check_decode_args(shape, num_splits);
   if (rc != PA_OK) return rc;
   if (shape->num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || (!out && !rows))
     return PA_ERR_ARG;
-  if (q8 && !v_scale) return PA_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (lse && !aligned(lse, 4)) ||
-      (q8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))))
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (lse && !aligned(lse, 4)))
     return PA_ERR_ARG;
   if (!(scale == scale)) return PA_ERR_ARG;
   DecodeGeometry g;
@@ -1038,8 +1032,6 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache,
   a.q = q;
   a.k_cache = static_cast<const unsigned char*>(k_cache);
   a.v_cache = static_cast<const unsigned char*>(v_cache);
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = out;
@@ -1123,7 +1115,7 @@ int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
                 const int32_t* block_tables, const int32_t* context_lens, float scale,
                 const pa_shape* shape, const RowsOut& rows, void* workspace,
                 size_t workspace_bytes, cudaStream_t st, int late, int max_sms) {
-  return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
+  return decode_impl(q, k_cache, v_cache, false, block_tables, context_lens, scale,
                      nullptr, nullptr, shape, 0, workspace, workspace_bytes, st, 0, &rows, late,
                      max_sms);
 }
@@ -1142,21 +1134,19 @@ extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
                          pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
                          void* workspace, size_t workspace_bytes, void* stream) {
   pa::NvtxRange nvtx_range("pa_decode");
-  return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
+  return decode_impl(q, k_cache, v_cache, false, block_tables, context_lens, scale,
                      out, lse, shape, num_splits, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), 0);
 }
 
-extern "C" int pa_decode_int8(const pa_bf16* q, const int8_t* k_cache, const int8_t* v_cache,
-                              const float* k_scale, const float* v_scale,
+extern "C" int pa_decode_int8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
                               const int32_t* block_tables, const int32_t* context_lens,
                               float scale, pa_bf16* out, float* lse, const pa_shape* shape,
                               int num_splits, void* workspace, size_t workspace_bytes,
                               void* stream) {
   pa::NvtxRange nvtx_range("pa_decode_int8");
-  if (!k_scale || !v_scale) return PA_ERR_ARG;
-  return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
-                     out, lse, shape, num_splits, workspace, workspace_bytes,
+  return decode_impl(q, k_cache, v_cache, true, block_tables, context_lens, scale, out, lse,
+                     shape, num_splits, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), 0);
 }
 
@@ -1189,7 +1179,7 @@ extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
   // with new tokens, the cache write ran just before: the decode prologue
   // (which reads only context_lens and block_tables) and every tile but the
   // segments' last ones may overlap it
-  return decode_impl(q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale,
+  return decode_impl(q, k_cache, v_cache, false, block_tables, context_lens, scale,
                      out, lse, shape, 0, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), num_new_tokens > 0 ? 1 : 0);
 }

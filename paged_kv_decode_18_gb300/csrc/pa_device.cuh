@@ -15,6 +15,11 @@ namespace pa {
 constexpr int kHeadDim = 128;                        // built head_dim
 constexpr int kBlock = 16;                           // built block_size (tokens)
 constexpr int kTileBytes = kBlock * kHeadDim * 2;    // one (block, kv head) K or V tile
+// one (block, kv head) tile of the int8 pool: 16 x 128 codes, then the 16 rows'
+// fp32 scales (a multiple of 16 bytes, so every tile is a bulk-copy source)
+constexpr int kInt8TileBytes = kBlock * kHeadDim + kBlock * 4;
+static_assert(kInt8TileBytes == PA_INT8_TILE_BYTES, "int8 tile layout");
+static_assert(kInt8TileBytes % 16 == 0, "int8 tiles must stay 16-byte aligned");
 constexpr unsigned kFull = 0xffffffffu;
 
 // Time limit of every wait on an asynchronous copy. A copy that has not landed

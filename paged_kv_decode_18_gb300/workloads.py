@@ -35,6 +35,8 @@ import torch
 
 POOL_SENTINEL_BITS = 0x7FC0  # bf16 quiet NaN
 POOL_SENTINEL_CODE = -128    # int8 pools
+INT8_CODE_BYTES = 16 * 128   # codes of one (block, KV head) tile of the int8 pool
+INT8_TILE_BYTES = INT8_CODE_BYTES + 16 * 4  # then the 16 rows' fp32 scales
 
 NUM_Q_HEADS = 16
 NUM_KV_HEADS = 8
@@ -91,13 +93,15 @@ class Workload:
         return pool, pool.clone()
 
     def empty_pool_i8(self, device="cpu"):
-        """An int8 pool (k codes, v codes, k scales, v scales). Unwritten codes
-        hold -128 (never produced by the quantiser) and unwritten scales NaN."""
-        codes = torch.full(self.pool_shape(), POOL_SENTINEL_CODE, dtype=torch.int8,
-                           device=device)
-        scales = torch.full(self.pool_shape()[:3], float("nan"), dtype=torch.float32,
-                            device=device)
-        return codes, codes.clone(), scales, scales.clone()
+        """An int8 pool pair (k, v) in the library's tile layout, uint8
+        [NB, Hkv, 2112]: each (block, KV head) tile holds its 16 x 128 codes,
+        then its 16 fp32 row scales. Unwritten codes hold -128 (never produced
+        by the quantiser) and unwritten scales NaN."""
+        NB, H, BS, D = self.pool_shape()
+        codes = torch.full((NB, H, BS, D), POOL_SENTINEL_CODE, dtype=torch.int8)
+        scales = torch.full((NB, H, BS), float("nan"), dtype=torch.float32)
+        t = int8_pool_pack(codes, scales).to(device)
+        return t, t.clone()
 
 
 def _randn_bf16(g: torch.Generator, shape) -> torch.Tensor:
@@ -318,6 +322,25 @@ def mixed(seed: int = 0, num_verify: int = 48, verify_q: int = 5, lo: int = 256,
         ql.append(prefill_chunk)
     return build("mixed", seed, ctx, ql, pool_factor=pool_factor,
                  meta={"config": "mixed verify + chunked prefill"})
+
+
+def int8_pool_pack(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """(codes int8 [NB, H, 16, 128], scales fp32 [NB, H, 16]) -> the tile
+    layout, uint8 [NB, H, 2112] (codes, then scales, per tile). Layout only."""
+    NB, H = codes.shape[:2]
+    t = torch.empty((NB, H, INT8_TILE_BYTES), dtype=torch.uint8, device=codes.device)
+    t[..., :INT8_CODE_BYTES] = codes.contiguous().view(torch.uint8).reshape(NB, H, -1)
+    t[..., INT8_CODE_BYTES:] = scales.contiguous().view(torch.uint8).reshape(NB, H, -1)
+    return t
+
+
+def int8_pool_split(t: torch.Tensor):
+    """The tile layout uint8 [NB, H, 2112] -> (codes int8 [NB, H, 16, 128],
+    scales fp32 [NB, H, 16]), copies. Layout only."""
+    NB, H = t.shape[:2]
+    codes = t[..., :INT8_CODE_BYTES].contiguous().view(torch.int8).reshape(NB, H, 16, 128)
+    scales = t[..., INT8_CODE_BYTES:].contiguous().view(torch.float32)
+    return codes, scales
 
 
 CONFIGS = {

@@ -5,6 +5,7 @@ import numpy as np
 import torch
 
 from paged_kv_decode_18_gb300 import binding as B
+from paged_kv_decode_18_gb300 import workloads as W
 
 OUT_ATOL = 1e-2
 OUT_RTOL = 1e-2
@@ -69,6 +70,14 @@ class DeviceBatch:
         return out, lse
 
 
+def int8_pools_numpy(kc, vc):
+    """Device int8 pools in the tile layout -> (k codes, v codes, k scales,
+    v scales) numpy arrays, the oracle's form."""
+    kcodes, kscales = W.int8_pool_split(kc.cpu())
+    vcodes, vscales = W.int8_pool_split(vc.cpu())
+    return kcodes.numpy(), vcodes.numpy(), kscales.numpy(), vscales.numpy()
+
+
 class Int8Batch:
     """A workload on the GPU with its int8 pool written by the CUDA quantising
     cache write (history first, then the step's new tokens)."""
@@ -76,19 +85,20 @@ class Int8Batch:
     def __init__(self, w):
         dev = device()
         self.w, self.dev = w, dev
-        self.kc, self.vc, self.ks, self.vs = w.empty_pool_i8(dev)
+        self.kc, self.vc = w.empty_pool_i8(dev)
         if w.k_hist.shape[0]:
             B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                        self.kc, self.vc, self.ks, self.vs)
+                                        self.kc, self.vc)
         B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev),
-                                    self.kc, self.vc, self.ks, self.vs)
+                                    self.kc, self.vc)
         self.q = w.q.to(dev)
         self.bt = w.block_tables.to(dev)
         self.cl = w.context_lens.to(dev)
 
     def pools(self):
-        return (self.kc.cpu().numpy(), self.vc.cpu().numpy(), self.ks.cpu().numpy(),
-                self.vs.cpu().numpy())
+        """(k codes, v codes, k scales, v scales) as numpy, split out of the
+        tile layout."""
+        return int8_pools_numpy(self.kc, self.vc)
 
     def decode(self, num_splits=0, with_lse=True):
         out = torch.empty_like(self.q)
@@ -96,8 +106,8 @@ class Int8Batch:
             if with_lse else None
         sh = B.shape_of(self.q, self.kc, self.bt)
         ws = B.workspace(B.pa_decode_int8_workspace_size(sh, num_splits), self.dev)
-        B.pa_decode_int8(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.cl,
-                         self.w.scale, out, lse, num_splits=num_splits, workspace=ws)
+        B.pa_decode_int8(self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale, out, lse,
+                         num_splits=num_splits, workspace=ws)
         return out, lse
 
 

@@ -94,10 +94,10 @@ def test_window_longer_than_context_is_flagged():
 def test_int8_bad_slot_and_block_are_flagged():
     w = W.tiny(seed=44)
     dev = torch.device("cuda:0")
-    kc, vc, ks, vs = w.empty_pool_i8(dev)
+    kc, vc = w.empty_pool_i8(dev)
     slots = w.slot_new.clone()
     slots[1] = w.num_blocks * w.block_size + 5
-    B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), slots.to(dev), kc, vc, ks, vs)
+    B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), slots.to(dev), kc, vc)
     torch.cuda.synchronize()
     assert B.pa_debug_read_error() & B.PA_DEVERR_SLOT_RANGE
     q = w.q.to(dev)
@@ -107,7 +107,6 @@ def test_int8_bad_slot_and_block_are_flagged():
     out = torch.empty_like(q)
     sh = B.shape_of(q, kc, bt)
     ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
-    B.pa_decode_int8(q, kc, vc, ks, vs, bt, w.context_lens.to(dev), w.scale, out, None,
-                     workspace=ws)
+    B.pa_decode_int8(q, kc, vc, bt, w.context_lens.to(dev), w.scale, out, None, workspace=ws)
     torch.cuda.synchronize()
     assert B.pa_debug_read_error() & B.PA_DEVERR_BLOCK_RANGE

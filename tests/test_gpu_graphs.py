@@ -105,9 +105,9 @@ def test_int8_write_and_decode_graph_replay():
     # new rows and the queries change in place
     w = W.engine(seed=63, num_seqs=24, context=300)
     dev = torch.device("cuda:0")
-    kc, vc, ks, vs = w.empty_pool_i8(dev)
+    kc, vc = w.empty_pool_i8(dev)
     B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                kc, vc, ks, vs)
+                                kc, vc)
     k_new, v_new, slots = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
     q, bt, cl = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
     out = torch.empty_like(q)
@@ -116,8 +116,8 @@ def test_int8_write_and_decode_graph_replay():
     ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
 
     def step():
-        B.pa_reshape_and_cache_int8(k_new, v_new, slots, kc, vc, ks, vs)
-        B.pa_decode_int8(q, kc, vc, ks, vs, bt, cl, w.scale, out, lse, workspace=ws)
+        B.pa_reshape_and_cache_int8(k_new, v_new, slots, kc, vc)
+        B.pa_decode_int8(q, kc, vc, bt, cl, w.scale, out, lse, workspace=ws)
 
     step()
     torch.cuda.synchronize()

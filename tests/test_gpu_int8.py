@@ -10,7 +10,7 @@ import torch
 from paged_kv_decode_18_gb300 import binding as B
 from paged_kv_decode_18_gb300 import build as libbuild
 from paged_kv_decode_18_gb300 import workloads as W
-from tests.gpu_util import Int8Batch, assert_attention_close, device
+from tests.gpu_util import Int8Batch, assert_attention_close, device, int8_pools_numpy
 from tests.pools import oracle_attention_i8, oracle_pools_i8
 
 pytestmark = pytest.mark.gpu
@@ -44,7 +44,7 @@ def test_int8_cache_write_bit_exact(name, sizes):
 def test_int8_cache_write_zero_rows_and_padding():
     w = W.make("tiny", seed=22)
     dev = device()
-    kc, vc, ks, vs = w.empty_pool_i8(dev)
+    kc, vc = w.empty_pool_i8(dev)
     k = w.k_new.clone()
     v = w.v_new.clone()
     k[0] = 0  # whole rows of zeros -> codes 0, scale 0
@@ -52,7 +52,7 @@ def test_int8_cache_write_zero_rows_and_padding():
     k[2, 1, 5] = 3e4  # an outlier in one row
     slots = w.slot_new.clone()
     slots[3] = -1  # padding: skipped
-    B.pa_reshape_and_cache_int8(k.to(dev), v.to(dev), slots.to(dev), kc, vc, ks, vs)
+    B.pa_reshape_and_cache_int8(k.to(dev), v.to(dev), slots.to(dev), kc, vc)
     torch.cuda.synchronize()
     assert B.pa_debug_read_error() == 0
     from oracle import oracle
@@ -61,8 +61,7 @@ def test_int8_cache_write_zero_rows_and_padding():
     rks = np.full(w.pool_shape()[:3], np.nan, np.float32)
     rvs = rks.copy()
     oracle.reshape_and_cache_i8(k, v, slots, rk, rv, rks, rvs)
-    _same_pools((kc.cpu().numpy(), vc.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy()),
-                (rk, rv, rks, rvs))
+    _same_pools(int8_pools_numpy(kc, vc), (rk, rv, rks, rvs))
 
 
 CASES = {
