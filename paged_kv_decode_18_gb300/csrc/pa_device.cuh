@@ -483,6 +483,58 @@ __device__ inline PieceCut build_piece_cut(const PlanSmem& P, int Hkv, int max_w
   return c;
 }
 
+// The SMs of one pa_decode_varlen call split between its tensor-core prefill
+// grid and its verify grid when the two run side by side: the prefill grid
+// keeps K of its N CTAs (one per SM) and the verify grid works on the rest,
+// with K = ceil(N A / (A + N V)), which evens out the two halves' times under
+// a plain cost model: A = the prefill work in CTA-time (kSplitTileNs per 128
+// keys seen by a 128-row query tile), V = the verify grid's time on all N SMs
+// (512 bytes of K and V per key seen per KV head at kSplitBytesPerUs). Every
+// grid that needs K computes it from the same inputs with the same integer
+// arithmetic, so they agree. Sequences with q_len >= min_lq are prefill. All
+// threads of the CTA call it (two CTA barriers); red: two 8-byte-aligned
+// words of shared memory. Returns 0 (no prefill work) .. N (no verify work).
+// A prefill tile beside the HBM-bound verify grid takes longer than alone
+// (1.46 us: its K/V loads from L2 wait behind the verify stream); a sweep of
+// this constant on the mixed batch (48 verify windows + two 512-token chunks)
+// put the best split at 2.25-3.0 us per tile (176-179 us per call against
+// 193 us with the grids in turn) and a cliff below it (2.0 us: 188 us), so the
+// constant sits on the safe side.
+constexpr long long kSplitTileNs = 2500;
+constexpr long long kSplitBytesPerUs = 5900000;  // verify grid on all SMs (HBM)
+
+__device__ inline int overlap_split(const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                    int S, int Hkv, int G, int causal, int min_lq, int max_ctx,
+                                    int N, unsigned long long* red) {
+  if (threadIdx.x == 0) red[0] = red[1] = 0ull;
+  __syncthreads();
+  unsigned long long pf = 0, vf = 0;  // keys seen, summed over query tiles (one KV head)
+  const int qt_pf = 128 / G, qt_v = 16 / G;  // query tokens per tile of either grid
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const int c = min(max(context_lens[s], 0), max_ctx);
+    const int lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
+    if (lq <= 0 || c <= 0 || (causal && lq > c)) continue;
+    const int qt = lq >= min_lq ? qt_pf : qt_v;
+    const long long nq = (lq + qt - 1) / qt;
+    // causal: query tile j sees c - lq + min(qt (j + 1), lq) keys
+    const long long keys =
+        causal ? nq * (c - lq) + (long long)qt * nq * (nq - 1) / 2 + lq : nq * (long long)c;
+    if (lq >= min_lq)
+      pf += (unsigned long long)keys;
+    else
+      vf += (unsigned long long)keys;
+  }
+  if (pf) atomicAdd(&red[0], pf);
+  if (vf) atomicAdd(&red[1], vf);
+  __syncthreads();
+  const long long A = (long long)red[0] * Hkv * kSplitTileNs / 128;
+  const long long V = (long long)red[1] * Hkv * 512 * 1000 / kSplitBytesPerUs;
+  if (A == 0) return 0;
+  if (V == 0) return N;
+  const long long K = ((long long)N * A + A + (long long)N * V - 1) / (A + (long long)N * V);
+  return (int)(K < 1 ? 1 : (K > N - 1 ? N - 1 : K));
+}
+
 // The merge a worker boundary owns. A segment (pair, kv head) cut by range
 // boundaries is merged by the first boundary inside it: boundary w owns the
 // segment containing tile range_start(w) when that segment began inside worker

@@ -193,7 +193,7 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
                       int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
                       const pa_shape* sh, void* workspace, cudaStream_t st,
                       int min_q_len = kTcMinQLen, const RowsOut* rows = nullptr,
-                      const int32_t* row_map = nullptr, int parts = 3);
+                      const int32_t* row_map = nullptr, int parts = 3, int split = 0);
 // parts: bit 0 launches the attention grid, bit 1 its merge grid.
 
 // Each TU that owns kernels exposes the reader of its device error word.

@@ -87,6 +87,9 @@ struct TcArgs {
   int causal;
   int npairs_cap;
   int num_workers;
+  // > 0: this grid runs beside the verify grid of the same call and keeps
+  // overlap_split(...) of its split CTAs (one per SM); the others leave at once
+  int split;
   int min_lq;
   float* part_o;    // [NW * 2][128 rows][128]
   float* part_lse;  // [NW * 2][128 rows]
@@ -261,6 +264,22 @@ __device__ __forceinline__ int* cut_view(unsigned char* base, const TcArgs& a) {
   return reinterpret_cast<int*>(base) + (a.npairs_cap + 1) + 3 * (a.S + 1);
 }
 
+// Two words for the SM split's reduction, after the cut (8-byte aligned).
+__device__ __forceinline__ unsigned long long* split_view(unsigned char* base, const TcArgs& a) {
+  const uintptr_t p = reinterpret_cast<uintptr_t>(cut_view(base, a) + a.num_workers + 1);
+  return reinterpret_cast<unsigned long long*>((p + 7) & ~uintptr_t(7));
+}
+
+// The CTAs this call's prefill grid works with (all of them unless it runs
+// beside the verify grid).
+__device__ __forceinline__ int prefill_workers(const TcArgs& a, unsigned char* plan_base) {
+  if (a.split <= 0) return a.num_workers;
+  const int K = overlap_split(a.cu_seqlens_q, a.context_lens, a.S, a.Hkv, a.G, a.causal,
+                              a.min_lq, a.max_blocks * kBlock, a.split,
+                              split_view(plan_base, a));
+  return min(a.num_workers, K);
+}
+
 __global__ void __launch_bounds__(kThreadsT, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                             const __grid_constant__ CUtensorMap tmk,
@@ -292,10 +311,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
   // launched as a programmatic dependent of the previous grid
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int max_workers = prefill_workers(a, smem + kOffPlan);
+  // beside a verify grid: the CTAs past the split leave now, freeing their SMs
+  if ((int)blockIdx.x >= max_workers) return;
   PlanInputs in;
   plan_inputs(a, in);
   build_plan(in, P, nullptr);  // ends with a CTA barrier
-  const PieceCut cut = build_piece_cut(P, Hkv, a.num_workers, kPieceCost4, cut_view(smem + kOffPlan, a));
+  const PieceCut cut = build_piece_cut(P, Hkv, max_workers, kPieceCost4, cut_view(smem + kOffPlan, a));
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int w = blockIdx.x;
@@ -704,8 +726,9 @@ __global__ void __launch_bounds__(kFixThreads)
   plan_view(fx_smem, a, P);
   PlanInputs in;
   plan_inputs(a, in);
+  const int max_workers = prefill_workers(a, fx_smem);
   build_plan(in, P, nullptr);
-  const PieceCut cut = build_piece_cut(P, a.Hkv, a.num_workers, kPieceCost4, cut_view(fx_smem, a));
+  const PieceCut cut = build_piece_cut(P, a.Hkv, max(max_workers, 1), kPieceCost4, cut_view(fx_smem, a));
   const int w = blockIdx.x;
   const MergeJob job = merge_job_of(P, a.S, a.Hkv, w, cut.nw, cut);
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -798,9 +821,9 @@ bool make_q_map(CUtensorMap* map, const void* q, int64_t num_q_tokens, int Hq, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// plan arrays, then the worker starts of the cut
+// plan arrays, then the worker starts of the cut, then the split's two words
 size_t plan_bytes(int S, int npairs_cap, int workers) {
-  return sizeof(int) * ((size_t)npairs_cap + 1 + 3 * ((size_t)S + 1) + (size_t)workers + 1);
+  return sizeof(int) * ((size_t)npairs_cap + 1 + 3 * ((size_t)S + 1) + (size_t)workers + 1) + 24;
 }
 
 }  // namespace
@@ -846,7 +869,7 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
                       const int32_t* context_lens, const int32_t* cu_seqlens_q,
                       int64_t num_q_tokens, int causal, float scale, pa_bf16* out, float* lse,
                       const pa_shape* sh, void* workspace, cudaStream_t st, int min_q_len,
-                      const RowsOut* rows, const int32_t* row_map, int parts) {
+                      const RowsOut* rows, const int32_t* row_map, int parts, int split) {
   const int G = sh->num_q_heads / sh->num_kv_heads;
   CUtensorMap tmq, tmk, tmv;
   const int64_t pool_rows = sh->num_blocks * sh->num_kv_heads * kBlock;
@@ -871,6 +894,7 @@ int launch_prefill_tc(const PrefillTcGeometry& g, const pa_bf16* q, const pa_bf1
   a.causal = causal ? 1 : 0;
   a.npairs_cap = g.npairs_cap;
   a.num_workers = g.workers;
+  a.split = split > 0 ? g.grid : 0;
   a.min_lq = min_q_len;
   if (rows) a.rows = *rows;
   a.row_map = row_map;

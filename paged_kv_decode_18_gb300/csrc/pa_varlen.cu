@@ -64,6 +64,10 @@ struct VarlenArgs {
   // nothing it reads, so verify tiles stream on the SMs that the prefill
   // grid's tail leaves free
   int late;
+  // > 0 (with late): the prefill grid ahead runs beside this one on K of its
+  // `split` CTAs (overlap_split); this grid works on the other SMs' share of
+  // its CTAs, the first ones launched
+  int split;
 };
 
 // byte offset of (row, 16-byte chunk) inside a 16 x 128 B box written by TMA
@@ -125,12 +129,24 @@ __device__ __forceinline__ void varlen_body(const CUtensorMap& tmk, const CUtens
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int W = P.total;
-  // ranges are dealt out transposed (range w = warp * gridDim.x + CTA):
-  // neighbouring ranges -- often the same kind of work (verify tiles streaming
-  // from HBM, or prefill tiles from L2) -- land on different CTAs and SMs, so
-  // each SM gets a mix
-  const int w = warp * (int)gridDim.x + (int)blockIdx.x;
-  const int nw = min(a.num_workers, W);
+  // CTAs that take work: all, or beside a prefill grid that keeps K of N
+  // SMs, the share of the other N - K (the CTAs launched first)
+  int ctas = (int)gridDim.x;
+  if (a.split > 0) {
+    const uintptr_t r = reinterpret_cast<uintptr_t>(scratch);
+    const int K = overlap_split(a.cu_seqlens_q, a.context_lens, S, Hkv, G, a.causal,
+                                a.max_lq + 1, a.max_blocks * kBlock, a.split,
+                                reinterpret_cast<unsigned long long*>((r + 7) & ~uintptr_t(7)));
+    ctas = max(1, (int)(((int64_t)gridDim.x * (a.split - K)) / a.split));
+  }
+  // ranges are dealt out transposed (range w = warp * ctas + CTA):
+  // neighbouring ranges -- often the same kind of work -- land on different
+  // CTAs and SMs, so each SM gets a mix; the CTAs past `ctas` hold the
+  // remaining (empty) worker slots
+  const int w = (int)blockIdx.x < ctas
+                    ? warp * ctas + (int)blockIdx.x
+                    : ctas * NWARPS + ((int)blockIdx.x - ctas) * NWARPS + warp;
+  const int nw = min(ctas * NWARPS, W);
   int R0 = 0, R1 = 0;
   if (w < nw) {
     R0 = (int)((int64_t)w * W / nw);
@@ -676,17 +692,21 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   // Sequences with long query chunks (prefill) run as tcgen05 tiles of 128
   // rows, the others (verify) on the mma.sync kernel; the prefill grid goes
   // first. When the batch surely holds short sequences (fewer than
-  // kTcMinQLen query tokens per sequence on average), the verify grid follows
-  // it as a late dependent, so verify CTAs start on each SM that the prefill
-  // grid's tail frees, and the prefill merge moves behind the verify grid.
+  // kTcMinQLen query tokens per sequence on average), the two grids run side
+  // by side: the prefill grid keeps the K of its CTAs that overlap_split
+  // gives (one per SM; the rest leave at once), the verify grid follows it as
+  // a late dependent and deals its work to the CTAs that land on the other
+  // SMs, and the prefill merge moves behind the verify grid.
   // Otherwise (prefill-only batches) the prefill merge follows its own grid
   // directly, one grid-completion hop earlier.
   const bool overlap = tg.enabled && num_q_tokens < (int64_t)kTcMinQLen * shape->num_seqs;
   a.late = overlap ? 1 : 0;
+  a.split = overlap ? tg.grid : 0;
   if (tg.enabled) {
     rc = launch_prefill_tc(tg, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
                            num_q_tokens, causal, scale, out, lse, shape, ws + g.ws_bytes, st,
-                           kTcMinQLen, nullptr, nullptr, /*parts=*/overlap ? 1 : 3);
+                           kTcMinQLen, nullptr, nullptr, /*parts=*/overlap ? 1 : 3,
+                           /*split=*/overlap ? 1 : 0);
     if (rc != PA_OK) return rc;
   }
   if (launch_dependent(paged_varlen_kernel<kWarps, kStages>, dim3(g.grid), dim3(kWarps * 32),
@@ -695,7 +715,7 @@ extern "C" int pa_decode_varlen(const pa_bf16* q, const pa_bf16* k_cache, const 
   if (overlap) {
     rc = launch_prefill_tc(tg, q, k_cache, v_cache, block_tables, context_lens, cu_seqlens_q,
                            num_q_tokens, causal, scale, out, lse, shape, ws + g.ws_bytes, st,
-                           kTcMinQLen, nullptr, nullptr, /*parts=*/2);
+                           kTcMinQLen, nullptr, nullptr, /*parts=*/2, /*split=*/1);
     if (rc != PA_OK) return rc;
   }
   if (launch_dependent(varlen_fixup_kernel, dim3(g.workers), dim3(kFixWarps * 32), 0, st,
