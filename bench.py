@@ -397,11 +397,21 @@ def measure_decode(name, w, dev, B, args, layers, splits=(0,), world=1, clocks=N
 
 
 def run_e2e(args, bench):
-    """The step through the public calls with host buffers: the step's inputs
-    (q, new K/V, slots, block tables, context lengths) staged in one pinned
-    buffer and copied host-to-device in one copy, the library call, and out +
-    lse (views of one device buffer) copied back in one copy and read on the
-    host, every step."""
+    """The step through the public calls with host buffers, every step: the
+    step's inputs (q, new K/V, slots, block tables, context lengths) staged in
+    one pinned buffer and copied host-to-device in one copy, the library call,
+    and out + lse (views of one device buffer) copied back in one copy and
+    read on the host.
+
+    `value` runs a forward of the layer steps as an engine captures it: one
+    CUDA graph holding every layer's step, each step's upload on a side
+    stream overlapping the previous step's call and its download on another
+    side stream after its call (two sets of device staging buffers, events
+    ordering their reuse, one pinned result slot per step); the host replays
+    it and reads every step's result, host-timed over whole forwards.
+    `serial_value` runs copy, call, copy back and a stream sync one after the
+    other through the binding; `graph_value` is that serial step captured in
+    a CUDA graph per layer."""
     w, dev, B = bench.w, bench.dev, bench.B
     names = ("q", "k_new", "v_new", "slot_new", "block_tables", "context_lens")
 
@@ -418,31 +428,104 @@ def run_e2e(args, bench):
         return buf, views
 
     src = [getattr(w, k).contiguous() for k in names]
-    host_in, host_views = packed(src, "cpu", True)
-    for v, t in zip(host_views, src):
-        v.copy_(t)
-    dev_in, dv = packed(src, dev, False)
-    d = dict(zip(names, dv))
     outs = [torch.empty(w.q.shape, dtype=torch.bfloat16),
             torch.empty(w.q.shape[:2], dtype=torch.float32)]
-    dev_out, (out, lse) = packed(outs, dev, False)
-    host_out, _ = packed(outs, "cpu", True)
     n = len(bench.pools)
     stream = torch.cuda.current_stream()
-
-    def prepared(st):
-        return [B.prepare_append_decode(d["k_new"], d["v_new"], d["slot_new"], d["q"], kc, vc,
-                                        d["block_tables"], d["context_lens"], w.scale, out, lse,
-                                        workspace=bench.workspace(0), stream=st)
-                for kc, vc in bench.pools]
-    calls = prepared(stream)       # eager: bound to this stream
-    calls_graph = prepared(None)   # captured: the capture stream at capture time
+    nbuf = 2
+    host_in, dev_in, host_out, dev_out, calls_b, views = [], [], [], [], [], []
+    for _ in range(nbuf):
+        hb, hv = packed(src, "cpu", True)
+        for v, t in zip(hv, src):
+            v.copy_(t)
+        db, dv = packed(src, dev, False)
+        do, (out, lse) = packed(outs, dev, False)
+        ho, _ = packed(outs, "cpu", True)
+        d = dict(zip(names, dv))
+        views.append((d, out, lse))
+        host_in.append(hb)
+        dev_in.append(db)
+        host_out.append(ho)
+        dev_out.append(do)
+        calls_b.append([B.prepare_append_decode(d["k_new"], d["v_new"], d["slot_new"], d["q"],
+                                                kc, vc, d["block_tables"], d["context_lens"],
+                                                w.scale, out, lse, workspace=bench.workspace(0),
+                                                stream=stream)
+                        for kc, vc in bench.pools])
+    # One forward of the n layer steps, pipelined and captured in one CUDA
+    # graph: step i's upload runs on a side stream while step i-1 computes,
+    # its download on another side stream after its call, each into its own
+    # pinned slot; events order the reuse of the two device buffer sets. The
+    # host replays the graph and then reads every step's result.
     steps = max(1, min(args.steps, 2000))
+    host_outs = [packed(outs, "cpu", True)[0] for _ in range(n)]
+    sink = [0.0]
+    calls_gb = []
+    for b in range(nbuf):
+        d, out, lse = views[b]
+        calls_gb.append([B.prepare_append_decode(d["k_new"], d["v_new"], d["slot_new"], d["q"],
+                                                 kc, vc, d["block_tables"], d["context_lens"],
+                                                 w.scale, out, lse,
+                                                 workspace=bench.workspace(0), stream=None)
+                         for kc, vc in bench.pools])
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_done = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    fwd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(fwd):
+        cap = torch.cuda.current_stream()
+        up.wait_stream(cap)
+        down.wait_stream(cap)
+        for i in range(n):
+            b = i % nbuf
+            with torch.cuda.stream(up):
+                if i >= nbuf:
+                    up.wait_event(ev_done[i - nbuf])  # step i-2 is done with dev_in[b]
+                dev_in[b].copy_(host_in[b], non_blocking=True)
+                ev_in[i].record(up)
+            cap.wait_event(ev_in[i])
+            if i >= nbuf:
+                cap.wait_event(ev_out[i - nbuf])  # step i-2's result has left dev_out[b]
+            calls_gb[b][i]()
+            ev_done[i].record(cap)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done[i])
+                host_outs[i].copy_(dev_out[b], non_blocking=True)
+                ev_out[i].record(down)
+        cap.wait_stream(up)
+        cap.wait_stream(down)
+
+    def forward():
+        fwd.replay()
+        stream.synchronize()
+        for i in range(n):
+            sink[0] += float(host_outs[i][0])  # every step's result is read on the host
+
+    reps = max(1, -(-steps // n))
+    for _ in range(max(2, -(-min(args.warmup, 56) // n))):
+        forward()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        forward()
+    ms = (time.perf_counter() - t0) * 1e3
+    res = {"value": w.num_q_tokens * reps * n / (ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": host_in[0].numel(), "d2h_bytes_per_step": host_outs[0].numel(),
+           "steps": reps * n, "ms_per_step": ms / (reps * n),
+           "path": "prepared pa_append_decode call through the Python binding; every step "
+                   "copies its inputs in (one H2D copy from pinned memory) and its out + lse "
+                   "back (one D2H copy), and the host reads every result; the n layer steps of "
+                   "a forward are captured in one CUDA graph with the uploads and downloads on "
+                   "side streams overlapping the calls; host-timed over whole forwards"}
+
+    # serial: copy in, call, copy back, sync, every step
+    hb, db, ho, do, calls = host_in[0], dev_in[0], host_out[0], dev_out[0], calls_b[0]
 
     def step(i):
-        dev_in.copy_(host_in, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
         calls[i % n]()
-        host_out.copy_(dev_out, non_blocking=True)
+        ho.copy_(do, non_blocking=True)
         stream.synchronize()  # the result is read on the host
 
     for i in range(max(3, min(args.warmup, 50))):
@@ -454,22 +537,22 @@ def run_e2e(args, bench):
         step(i)
     e.record()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e)
-    res = {"value": w.num_q_tokens * steps / (ms / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": host_in.numel(), "d2h_bytes_per_step": host_out.numel(),
-           "steps": steps, "ms_per_step": ms / steps,
-           "path": "prepared pa_append_decode call through the Python binding, one H2D and "
-                   "one D2H copy and a stream sync per step"}
+    res["serial_value"] = w.num_q_tokens * steps / (s.elapsed_time(e) / 1e3)
 
-    # the same step as an engine runs it: the two copies and the call captured
-    # once in a CUDA graph per layer, replayed and read back every step
+    # the serial step as an engine captures it: the two copies and the call in
+    # a CUDA graph per layer, replayed and read back every step
+    d, out, lse = views[0]
+    calls_graph = [B.prepare_append_decode(d["k_new"], d["v_new"], d["slot_new"], d["q"], kc, vc,
+                                           d["block_tables"], d["context_lens"], w.scale, out,
+                                           lse, workspace=bench.workspace(0), stream=None)
+                   for kc, vc in bench.pools]  # the capture stream at capture time
     graphs = []
     for i in range(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            dev_in.copy_(host_in, non_blocking=True)
+            db.copy_(hb, non_blocking=True)
             calls_graph[i]()
-            host_out.copy_(dev_out, non_blocking=True)
+            ho.copy_(do, non_blocking=True)
         graphs.append(g)
     for i in range(max(3, min(args.warmup, 50))):
         graphs[i % n].replay()
