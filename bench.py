@@ -836,6 +836,8 @@ def run_case(args, dev):
     B.load()
     if args.case == "prefill":  # the chunked-prefill part of the mixed batch
         w = W.mixed(seed=args.seed, num_verify=0)
+    elif args.case == "prefill_long":  # two 2048-token chunks (contexts 2048 and 8192)
+        w = W.mixed(seed=args.seed, num_verify=0, prefill_chunk=2048, prefill_offsets=(0, 6144))
     elif args.case in ("ragged_int8", "engine_int8", "long_int8"):
         w = W.make(args.case[:-5], seed=args.seed)
     elif args.case == "shared_prompt":
@@ -856,7 +858,7 @@ def run_case(args, dev):
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
     sh = B.shape_of(q, kc, bt)
-    varlen = args.case in ("mixed", "prefill")
+    varlen = args.case in ("mixed", "prefill", "prefill_long")
     cascade = args.case == "shared_prompt"
     if varlen:
         ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, q.shape[0], w.max_q_len), dev)
@@ -946,7 +948,7 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["tiny", "engine", "ragged", "long", "mixed", "prefill",
+    ap.add_argument("--case", choices=["tiny", "engine", "ragged", "long", "mixed", "prefill", "prefill_long",
                                        "ragged_int8", "engine_int8", "long_int8",
                                        "shared_prompt"],
                     help="time one workload with eager calls (for profiling), nothing else")
