@@ -117,3 +117,59 @@ def test_prefill_segment_cut_into_many_pieces():
     ref, ref_lse = oracle_attention(w)
     assert_attention_close(out, lse, ref, ref_lse, what="many pieces")
     assert torch.equal(out, out_nl)
+
+
+def _varlen_max_q(db, max_q_len):
+    # pa_decode_varlen with a max_q_len above the batch's longest window (an
+    # upper bound is allowed)
+    out = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.dev)
+    sh = B.shape_of(db.q, db.kc, db.block_tables)
+    ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, db.q.shape[0], max_q_len), db.dev)
+    B.pa_decode_varlen(db.q, db.kc, db.vc, db.block_tables, db.context_lens, db.cu_seqlens_q,
+                       max_q_len, db.w.scale, out, lse, causal=True, workspace=ws)
+    return out, lse
+
+
+def test_side_by_side_split_one_prefill_cta():
+    # 59 verify windows over long contexts beside one 32-token chunk: the
+    # prefill grid keeps a single CTA, the verify grid the other SMs
+    ctx = [2000 + 37 * i for i in range(59)] + [32]
+    ql = [5] * 59 + [32]
+    w = W.build("split1", 41, ctx, ql, pool_factor=1.1)
+    db = DeviceBatch(w)
+    out, lse = db.varlen()
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="split K=1")
+
+
+def test_side_by_side_split_one_verify_cta():
+    # one 1024-token chunk and one short verify window beside 98 sequences
+    # with no queries (the batch still averages under 32 query tokens): the
+    # prefill grid keeps all but one CTA, the verify grid works on one
+    ctx = [4096, 16] + [16] * 98
+    ql = [1024, 5] + [0] * 98
+    w = W.build("splitN", 42, ctx, ql, pool_factor=1.1)
+    db = DeviceBatch(w)
+    out, lse = db.varlen()
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="split K=N-1")
+
+
+def test_side_by_side_split_no_prefill_work():
+    # only verify windows, with max_q_len declared above the tensor-core
+    # threshold: both grids launch, the prefill grid finds no work and leaves
+    # every SM to the verify grid
+    w = W.build("split0", 43, [300, 900, 40, 1500], [5, 7, 3, 9], pool_factor=1.2)
+    db = DeviceBatch(w)
+    out, lse = _varlen_max_q(db, 64)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention(w)
+    assert_attention_close(out, lse, ref, ref_lse, what="split K=0")
+    out2, lse2 = db.varlen()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
