@@ -30,10 +30,12 @@
 //             grows by more than 2^8 (exact either way); at the end of a piece
 //             the halves exchange (max, sum) through shared memory and write
 //             the normalised row during the next tile.
-// Work is the same equal cut of the batch's flat (query tile, KV head, key
-// tile) list used by the other kernels, at CTA granularity; pieces of a
-// segment cut between CTAs are merged by prefill_tc_fixup_kernel. Optional
-// fp32 row output with a row map serves the cascade's shared-prefix half.
+// Work is a cut of the batch's flat (query tile, KV head, key tile) list at
+// CTA granularity in which a segment start weighs as much as one key tile
+// (PieceCut); pieces of a segment cut between CTAs are merged by
+// prefill_tc_fixup_kernel. Beside a verify grid of the same call the grid
+// keeps only its share of the SMs (overlap_split). Optional fp32 row output
+// with a row map serves the cascade's shared-prefix half.
 #include <cudaTypedefs.h>
 
 #include "pa_device.cuh"
