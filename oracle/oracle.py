@@ -77,6 +77,18 @@ def _load():
         lib.pa_oracle_paged_attention_i8.restype = i32
         lib.pa_oracle_paged_attention_i8.argtypes = [
             P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, dbl, i32, i32, P, P]
+        lib.pa_oracle_e4m3_values.restype = i32
+        lib.pa_oracle_e4m3_values.argtypes = [P, i64, P]
+        lib.pa_oracle_e4m3_codes.restype = i32
+        lib.pa_oracle_e4m3_codes.argtypes = [P, i64, P]
+        lib.pa_oracle_quantize_rows_f8.restype = i32
+        lib.pa_oracle_quantize_rows_f8.argtypes = [P, i64, i32, P, P]
+        lib.pa_oracle_reshape_and_cache_f8.restype = i32
+        lib.pa_oracle_reshape_and_cache_f8.argtypes = [P, P, P, i64, i32, i32, i32, i64, P, P,
+                                                       P, P]
+        lib.pa_oracle_paged_attention_f8.restype = i32
+        lib.pa_oracle_paged_attention_f8.argtypes = [
+            P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, dbl, i32, i32, P, P]
         _lib = lib
         return lib
 
@@ -255,4 +267,83 @@ def paged_attention_i8(q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
         Hkv, D, BS, bt.shape[1], NB, float(scale), 1 if causal else 0, int(num_threads),
         _ptr(out), _ptr(lse))
     _check(rc, "paged_attention_i8")
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) pool: codes as uint8, one fp32 scale per (token, KV head) row
+# ---------------------------------------------------------------------------
+
+def e4m3_values(codes) -> np.ndarray:
+    """The value of each E4M3 code (uint8), fp64; NaN for the NaN codes."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, np.float64)
+    _check(_load().pa_oracle_e4m3_values(_ptr(c), c.size, _ptr(out)), "e4m3_values")
+    return out
+
+
+def e4m3_codes(y) -> np.ndarray:
+    """The finite E4M3 code nearest to each fp32 value (ties to the even code,
+    saturating at +-448)."""
+    a = np.ascontiguousarray(np.asarray(y, dtype=np.float32))
+    out = np.zeros(a.shape, np.uint8)
+    _check(_load().pa_oracle_e4m3_codes(_ptr(a), a.size, _ptr(out)), "e4m3_codes")
+    return out
+
+
+def quantize_rows_f8(x):
+    """bf16 rows [..., D] -> (codes uint8 [..., D], scales fp32 [...])."""
+    lib = _load()
+    x16 = _as_u16(x)
+    D = x16.shape[-1]
+    rows = x16.size // D
+    codes = np.zeros(x16.shape, np.uint8)
+    scales = np.zeros(x16.shape[:-1], np.float32)
+    _check(lib.pa_oracle_quantize_rows_f8(_ptr(x16), rows, D, _ptr(codes), _ptr(scales)),
+           "quantize_rows_f8")
+    return codes, scales
+
+
+def reshape_and_cache_f8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale) -> None:
+    """Quantising cache write into fp8 pools (numpy arrays, updated in place)."""
+    lib = _load()
+    k16, v16 = _as_u16(k), _as_u16(v)
+    sm = _as(slot_mapping, np.int64)
+    for a, dt in ((k_cache, np.uint8), (v_cache, np.uint8), (k_scale, np.float32),
+                  (v_scale, np.float32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise ValueError("fp8 pool arrays must be contiguous uint8 / float32")
+    T, Hkv, D = k16.shape
+    NB, Hkv2, BS, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or k_scale.shape != (NB, Hkv, BS):
+        raise ValueError("cache shape mismatch")
+    _check(lib.pa_oracle_reshape_and_cache_f8(_ptr(k16), _ptr(v16), _ptr(sm), T, Hkv, D, BS, NB,
+                                              _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                              _ptr(v_scale)), "reshape_and_cache_f8")
+
+
+def paged_attention_f8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                       cu_seqlens_q, scale: float, causal: bool = True, num_threads: int = 0):
+    """Paged attention in fp64 over fp8 pools (rows dequantised as value(code) * scale)."""
+    lib = _load()
+    q16 = _as_u16(q)
+    kc, vc = _as(k_cache, np.uint8), _as(v_cache, np.uint8)
+    ks, vs = _as(k_scale, np.float32), _as(v_scale, np.float32)
+    bt = _as(block_tables, np.int32)
+    cl = _as(context_lens, np.int32)
+    cu = _as(cu_seqlens_q, np.int32)
+    Tq, Hq, D = q16.shape
+    NB, Hkv, BS, D2 = kc.shape
+    if D2 != D or vc.shape != kc.shape or ks.shape != (NB, Hkv, BS) or vs.shape != ks.shape:
+        raise ValueError("cache shape mismatch")
+    S = cl.shape[0]
+    if bt.ndim != 2 or bt.shape[0] != S or cu.shape[0] != S + 1 or int(cu[-1]) != Tq:
+        raise ValueError("table / length shape mismatch")
+    out = np.zeros((Tq, Hq, D), np.float64)
+    lse = np.zeros((Tq, Hq), np.float64)
+    rc = lib.pa_oracle_paged_attention_f8(
+        _ptr(q16), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(cl), _ptr(cu), S, Hq,
+        Hkv, D, BS, bt.shape[1], NB, float(scale), 1 if causal else 0, int(num_threads),
+        _ptr(out), _ptr(lse))
+    _check(rc, "paged_attention_f8")
     return out, lse

@@ -49,6 +49,17 @@
  *   A row dequantises to code_d * scale (exact in fp64). Attention over an
  *   int8 pool is the attention above over the dequantised rows.
  *
+ *   FP8 KV rows (the same curriculum row names FP8 beside INT8; the format
+ *   is the OCP 8-bit float E4M3: 1 sign, 4 exponent bits with bias 7, 3
+ *   mantissa bits, no infinities, S.1111.111 = NaN, largest finite 448).
+ *   The plainest reading, as for INT8: one group per (token, KV head) row,
+ *     amax = max_d |x_d|;  amax == 0 -> all codes 0 and scale 0; else
+ *     inv = 448 / amax,  code_d = e4m3(x_d * inv),  scale = amax / 448,
+ *   each one IEEE fp32 operation, where e4m3(y) is the finite E4M3 value
+ *   nearest to y (ties to the even code, i.e. the even last mantissa bit)
+ *   and |y| beyond 448 gives +-448. A row dequantises to value(code_d) *
+ *   scale (exact in fp64).
+ *
  * Numbers: bf16 inputs are bit patterns (uint16). They are widened to fp64
  * exactly (bf16 -> fp32 is a 16-bit shift; fp32 -> fp64 is exact).
  */
@@ -142,6 +153,99 @@ static void quantize_row_i8(const uint16_t *x, int D, int8_t *codes, float *scal
         codes[d] = (int8_t)t;
     }
     *scale = amax / 127.0f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 codes (format and rule in the header).                           */
+/* ------------------------------------------------------------------------ */
+static double e4m3_value(uint8_t c) {
+    const int e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+/* the finite E4M3 code nearest to y, ties to the even code, saturating at 448:
+   a search over the 127 non-negative finite codes, in increasing order */
+static uint8_t e4m3_code(float y) {
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    const double a = fabs((double)y);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double d = fabs(e4m3_value((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best_d = d;
+            best = c;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+int pa_oracle_e4m3_values(const uint8_t *codes, int64_t n, double *values) {
+    if (n < 0) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) values[i] = e4m3_value(codes[i]);
+    return ORACLE_OK;
+}
+
+int pa_oracle_e4m3_codes(const float *y, int64_t n, uint8_t *codes) {
+    if (n < 0) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) codes[i] = e4m3_code(y[i]);
+    return ORACLE_OK;
+}
+
+static void quantize_row_f8(const uint16_t *x, int D, uint8_t *codes, float *scale) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(bf16_bits_to_float(x[d]));
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        for (int d = 0; d < D; ++d) codes[d] = 0;
+        *scale = 0.0f;
+        return;
+    }
+    const float inv = 448.0f / amax;
+    for (int d = 0; d < D; ++d) {
+        const float y = bf16_bits_to_float(x[d]) * inv;
+        codes[d] = e4m3_code(y);
+    }
+    *scale = amax / 448.0f;
+}
+
+/* rows [rows][D] bf16 -> codes [rows][D] e4m3, scales [rows] fp32 */
+int pa_oracle_quantize_rows_f8(const uint16_t *x, int64_t rows, int D, uint8_t *codes,
+                               float *scales) {
+    if (rows < 0 || D <= 0) return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        quantize_row_f8(x + r * D, D, codes + r * D, scales + r);
+    return ORACLE_OK;
+}
+
+/* Cache write into the fp8 pool, laid out as the int8 one. */
+int pa_oracle_reshape_and_cache_f8(const uint16_t *k, const uint16_t *v,
+                                   const int64_t *slot_mapping, int64_t num_tokens,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int64_t num_blocks, uint8_t *k_cache, uint8_t *v_cache,
+                                   float *k_scale, float *v_scale) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * (int64_t)block_size) return ORACLE_ERR_RANGE;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t src = (t * num_kv_heads + h) * (int64_t)head_dim;
+            int64_t row = (block * num_kv_heads + h) * (int64_t)block_size + offset;
+            quantize_row_f8(k + src, head_dim, k_cache + row * head_dim, k_scale + row);
+            quantize_row_f8(v + src, head_dim, v_cache + row * head_dim, v_scale + row);
+        }
+    }
+    return ORACLE_OK;
 }
 
 /* rows [rows][D] bf16 -> codes [rows][D] int8, scales [rows] fp32 */
@@ -291,7 +395,7 @@ int pa_oracle_attention_dense(const uint16_t *q, const uint16_t *K, const uint16
 /* ------------------------------------------------------------------------ */
 /* Pool element formats: bf16 (k16/v16) or int8 rows with one scale per row. */
 static int paged_attention_core(const uint16_t *q, const uint16_t *k16, const uint16_t *v16,
-                                const int8_t *k8, const int8_t *v8, const float *k_scale,
+                                const int8_t *k8, const int8_t *v8, int f8, const float *k_scale,
                                 const float *v_scale, const int32_t *block_tables,
                                 const int32_t *context_lens, const int32_t *cu_seqlens_q,
                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -353,6 +457,9 @@ static int paged_attention_core(const uint16_t *q, const uint16_t *k16, const ui
                 if (k16) {
                     K[p * D + d] = bf16_bits_to_double(k16[row + d]);
                     V[p * D + d] = bf16_bits_to_double(v16[row + d]);
+                } else if (f8) {  /* dequantised fp8 row: value(code) * scale */
+                    K[p * D + d] = e4m3_value((uint8_t)k8[row + d]) * (double)k_scale[srow];
+                    V[p * D + d] = e4m3_value((uint8_t)v8[row + d]) * (double)v_scale[srow];
                 } else {  /* dequantised int8 row: code * scale, exact in fp64 */
                     K[p * D + d] = (double)k8[row + d] * (double)k_scale[srow];
                     V[p * D + d] = (double)v8[row + d] * (double)v_scale[srow];
@@ -387,7 +494,7 @@ int pa_oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache,
                               int block_size, int max_blocks_per_seq, int64_t num_blocks,
                               double scale, int causal, int mode, int64_t tile,
                               int num_threads, double *out, double *lse) {
-    return paged_attention_core(q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_tables,
+    return paged_attention_core(q, k_cache, v_cache, NULL, NULL, 0, NULL, NULL, block_tables,
                                 context_lens, cu_seqlens_q, num_seqs, num_q_heads,
                                 num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                 num_blocks, scale, causal, mode, tile, num_threads, out, lse);
@@ -403,11 +510,28 @@ int pa_oracle_paged_attention_i8(const uint16_t *q, const int8_t *k_cache,
                                  double scale, int causal, int num_threads, double *out,
                                  double *lse) {
     if (!k_cache || !v_cache || !k_scale || !v_scale) return ORACLE_ERR_ARG;
-    return paged_attention_core(q, NULL, NULL, k_cache, v_cache, k_scale, v_scale,
+    return paged_attention_core(q, NULL, NULL, k_cache, v_cache, 0, k_scale, v_scale,
                                 block_tables, context_lens, cu_seqlens_q, num_seqs,
                                 num_q_heads, num_kv_heads, head_dim, block_size,
                                 max_blocks_per_seq, num_blocks, scale, causal, 0, 0,
                                 num_threads, out, lse);
+}
+
+/* Paged attention over an fp8 pool (rows dequantised as value(code) * scale). */
+int pa_oracle_paged_attention_f8(const uint16_t *q, const uint8_t *k_cache,
+                                 const uint8_t *v_cache, const float *k_scale,
+                                 const float *v_scale, const int32_t *block_tables,
+                                 const int32_t *context_lens, const int32_t *cu_seqlens_q,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                 double scale, int causal, int num_threads, double *out,
+                                 double *lse) {
+    if (!k_cache || !v_cache || !k_scale || !v_scale) return ORACLE_ERR_ARG;
+    return paged_attention_core(q, NULL, NULL, (const int8_t *)k_cache,
+                                (const int8_t *)v_cache, 1, k_scale, v_scale, block_tables,
+                                context_lens, cu_seqlens_q, num_seqs, num_q_heads,
+                                num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                num_blocks, scale, causal, 0, 0, num_threads, out, lse);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -35,6 +35,7 @@ import torch
 
 POOL_SENTINEL_BITS = 0x7FC0  # bf16 quiet NaN
 POOL_SENTINEL_CODE = -128    # int8 pools
+POOL_SENTINEL_F8 = 0x7F      # fp8 (E4M3) pools: a NaN code
 INT8_CODE_BYTES = 16 * 128   # codes of one (block, KV head) tile of the int8 pool
 INT8_TILE_BYTES = INT8_CODE_BYTES + 16 * 4  # then the 16 rows' fp32 scales
 
@@ -91,6 +92,16 @@ class Workload:
                           device=device)
         pool = pool.view(torch.bfloat16)
         return pool, pool.clone()
+
+    def empty_pool_f8(self, device="cpu"):
+        """An fp8 (E4M3) pool pair (k, v) in the same tile layout as the int8
+        pool, uint8 [NB, Hkv, 2112]. Unwritten codes hold 0x7F (a NaN code,
+        never produced by the quantiser) and unwritten scales NaN."""
+        NB, H, BS, D = self.pool_shape()
+        codes = torch.full((NB, H, BS, D), POOL_SENTINEL_F8, dtype=torch.uint8)
+        scales = torch.full((NB, H, BS), float("nan"), dtype=torch.float32)
+        t = int8_pool_pack(codes.view(torch.int8), scales).to(device)
+        return t, t.clone()
 
     def empty_pool_i8(self, device="cpu"):
         """An int8 pool pair (k, v) in the library's tile layout, uint8

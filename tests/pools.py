@@ -64,3 +64,25 @@ def oracle_attention_i8(w, pools=None, num_threads=0):
     return oracle.paged_attention_i8(w.q, kc, vc, ks, vs, w.block_tables, w.context_lens,
                                      w.cu_seqlens_q, w.scale, causal=w.causal,
                                      num_threads=num_threads)
+
+
+def oracle_pools_f8(w):
+    """(k codes, v codes, k scales, v scales) of the fp8 (E4M3) pool after the
+    oracle's quantising cache write of the history and the new tokens;
+    unwritten rows keep the sentinels (0x7F, NaN)."""
+    from paged_kv_decode_18_gb300.workloads import POOL_SENTINEL_F8
+    kc = np.full(w.pool_shape(), POOL_SENTINEL_F8, dtype=np.uint8)
+    vc = kc.copy()
+    ks = np.full(w.pool_shape()[:3], np.nan, dtype=np.float32)
+    vs = ks.copy()
+    if w.k_hist.shape[0]:
+        oracle.reshape_and_cache_f8(w.k_hist, w.v_hist, w.slot_hist, kc, vc, ks, vs)
+    oracle.reshape_and_cache_f8(w.k_new, w.v_new, w.slot_new, kc, vc, ks, vs)
+    return kc, vc, ks, vs
+
+
+def oracle_attention_f8(w, pools=None, num_threads=0):
+    kc, vc, ks, vs = oracle_pools_f8(w) if pools is None else pools
+    return oracle.paged_attention_f8(w.q, kc, vc, ks, vs, w.block_tables, w.context_lens,
+                                     w.cu_seqlens_q, w.scale, causal=w.causal,
+                                     num_threads=num_threads)
