@@ -93,7 +93,7 @@ def decode_algorithmic_bytes(w, unique: bool = False, kv_bytes_per_token: int | 
 
 
 def int8_bytes_per_token(w) -> int:
-    """int8 pool: 1-byte K and V codes plus one fp32 scale per (token, KV head)
+    """8-bit pools (int8, FP8): 1-byte K and V codes plus one fp32 scale per (token, KV head)
     row each (2112 B per token at 8 x 128)."""
     return w.num_kv_heads * (w.head_dim + 4) * 2
 
@@ -634,44 +634,54 @@ def run_secondary_varlen(w, dev, B, peak):
 
 
 def run_secondary_int8(ws_by_name, dev, B, peak):
-    """Decode over the INT8 pool (quantised cache write, fused dequant): the
-    engine and ragged batches rotated over the layer pools (as their bf16
-    lines are), and the long batch (one pool, larger than L2)."""
+    """Decode over the 8-bit pools (quantised cache write, fused dequant),
+    int8 and FP8 E4M3: the engine and ragged batches rotated over the layer
+    pools (as their bf16 lines are), and the long batch (one pool, larger
+    than L2)."""
+    fmts = {
+        "int8": (lambda w: w.empty_pool_i8(dev), B.pa_reshape_and_cache_int8,
+                 B.pa_decode_int8_workspace_size, B.pa_decode_int8,
+                 "int8 codes + fp32 row scales, one 2112-byte tile"),
+        "fp8": (lambda w: w.empty_pool_f8(dev), B.pa_reshape_and_cache_fp8,
+                B.pa_decode_fp8_workspace_size, B.pa_decode_fp8,
+                "FP8 E4M3 codes + fp32 row scales, one 2112-byte tile"),
+    }
     res = {}
-    for name, nlayers in (("engine", LAYERS), ("ragged", LAYERS), ("long", 1)):
-        w = ws_by_name[name]
-        pools = []
-        kh, vh, sh_ = w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev)
-        kn, vn, sn = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
-        for _ in range(nlayers):
-            kc, vc = w.empty_pool_i8(dev)
-            B.pa_reshape_and_cache_int8(kh, vh, sh_, kc, vc)
-            B.pa_reshape_and_cache_int8(kn, vn, sn, kc, vc)
-            pools.append((kc, vc))
-        del kh, vh, sh_
-        q = w.q.to(dev)
-        bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
-        out = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-        sh = B.shape_of(q, pools[0][0], bt)
-        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
-        ctr = [0]
+    for fmt, (empty, write, ws_size, decode, desc) in fmts.items():
+        for name, nlayers in (("engine", LAYERS), ("ragged", LAYERS), ("long", 1)):
+            w = ws_by_name[name]
+            pools = []
+            kh, vh, sh_ = w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev)
+            kn, vn, sn = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
+            for _ in range(nlayers):
+                kc, vc = empty(w)
+                write(kh, vh, sh_, kc, vc)
+                write(kn, vn, sn, kc, vc)
+                pools.append((kc, vc))
+            del kh, vh, sh_
+            q = w.q.to(dev)
+            bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
+            out = torch.empty_like(q)
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+            sh = B.shape_of(q, pools[0][0], bt)
+            ws = B.workspace(ws_size(sh, 0), dev)
+            ctr = [0]
 
-        def call():
-            kc, vc = pools[ctr[0] % nlayers]
-            ctr[0] += 1
-            B.pa_decode_int8(q, kc, vc, bt, cl, w.scale, out, lse, num_splits=0,
-                             workspace=ws)
-        ms = time_graph_calls(call, per_replay=4 if nlayers > 1 else 2)
-        alg = decode_algorithmic_bytes(w, unique=True, kv_bytes_per_token=int8_bytes_per_token(w))
-        gbs = alg / (ms / 1e3) / 1e9
-        res[f"{name}_int8"] = {"decode_ms": round(ms, 5), "alg_bytes": alg,
-                               "achieved_gbs": round(gbs, 1),
-                               "frac_of_measured_peak": round(gbs / peak, 4),
-                               "value": w.num_q_tokens / (ms / 1e3), "unit": UNIT,
-                               "kv_format": "int8 codes + fp32 row scales, one 2112-byte tile"}
-        del pools
-        torch.cuda.empty_cache()
+            def call():
+                kc, vc = pools[ctr[0] % nlayers]
+                ctr[0] += 1
+                decode(q, kc, vc, bt, cl, w.scale, out, lse, num_splits=0, workspace=ws)
+            ms = time_graph_calls(call, per_replay=4 if nlayers > 1 else 2)
+            alg = decode_algorithmic_bytes(w, unique=True,
+                                           kv_bytes_per_token=int8_bytes_per_token(w))
+            gbs = alg / (ms / 1e3) / 1e9
+            res[f"{name}_{fmt}"] = {"decode_ms": round(ms, 5), "alg_bytes": alg,
+                                    "achieved_gbs": round(gbs, 1),
+                                    "frac_of_measured_peak": round(gbs / peak, 4),
+                                    "value": w.num_q_tokens / (ms / 1e3), "unit": UNIT,
+                                    "kv_format": desc}
+            del pools
+            torch.cuda.empty_cache()
     return res
 
 

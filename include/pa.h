@@ -289,6 +289,49 @@ int pa_decode_int8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_ca
 size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_splits);
 
 /*
+ * FP8 KV cache (course pages, "The curriculum": the Machine layer names
+ * bf16/fp8 and the Memory & KV Cache layer quantization). The same tile
+ * layout as the int8 pool (PA_INT8_TILE_BYTES per (block, KV head): the
+ * block_size rows' codes, then their fp32 scales), with each code an OCP
+ * FP8 E4M3 byte: sign, 4 exponent bits (bias 7), 3 mantissa bits, no
+ * infinities, 0x7F / 0xFF = NaN, largest finite value 448.
+ *
+ * Row quantisation (group = one head row): amax = max_d |x_d|; if amax == 0
+ * every code is 0 and the scale 0; otherwise inv = fl(448 / amax),
+ * code_d = the E4M3 value nearest to fl(x_d * inv) (ties to the code with
+ * an even last mantissa bit; beyond +-448 it saturates to +-448),
+ * scale = fl(amax / 448). The writer never stores a NaN code. A row
+ * dequantises to value(code_d) * scale.
+ */
+
+/*
+ * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache_int8 with E4M3 codes
+ * (quantised as above). Same layout, alignment, slot rules and error bits;
+ * bf16 subnormal inputs are read as zero.
+ */
+int pa_reshape_and_cache_fp8(const pa_bf16* k, const pa_bf16* v, const int64_t* slot_mapping,
+                             int64_t num_tokens, uint8_t* k_cache, uint8_t* v_cache,
+                             const pa_shape* shape, void* stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode over the FP8 pool, dequantisation fused: each
+ * score is the decoded row's dot product times the row's K scale, and each
+ * softmax weight is multiplied by the row's V scale before it meets the
+ * decoded V row. Rows past a sequence's context are never read into the
+ * result (they may hold anything, NaN codes included). Same arguments,
+ * splits, outputs and workspace rules as pa_decode (workspace from
+ * pa_decode_fp8_workspace_size); k_cache and v_cache 16-byte aligned. The
+ * result is attention over the dequantised rows, within fp32 rounding.
+ */
+int pa_decode_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for pa_decode_fp8 with this shape and split choice. */
+size_t pa_decode_fp8_workspace_size(const pa_shape* shape, int num_splits);
+
+/*
  * pa_decode_cascade -- pa_decode (q_len 1, balanced) for a batch in which
  * groups of sequences share the physical blocks of a prompt prefix (prefix
  * caching: course README, "What to build in what order"; "S20 - The Complete
@@ -388,7 +431,7 @@ int pa_debug_read_error(void* stream);
 
 /*
  * pa_debug_inject_missing_copy -- failure-detection test hook. The next
- * decode launch (pa_decode, pa_append_decode, pa_decode_int8 or
+ * decode launch (pa_decode, pa_append_decode, pa_decode_int8, pa_decode_fp8 or
  * pa_decode_static_scratch) on this host thread leaves out the copy of flat
  * tile `flat_tile` of its work list (0 = the first (sequence 0, KV head 0,
  * block 0) tile), so the warp that waits for it runs into its bounded wait

@@ -44,6 +44,9 @@ EXPORTED = (
     "pa_reshape_and_cache_int8",
     "pa_decode_int8",
     "pa_decode_int8_workspace_size",
+    "pa_reshape_and_cache_fp8",
+    "pa_decode_fp8",
+    "pa_decode_fp8_workspace_size",
     "pa_decode_cascade",
     "pa_decode_cascade_ex",
     "pa_decode_cascade_workspace_size",
@@ -111,6 +114,12 @@ def load(path: str | None = None):
         lib.pa_decode_int8.argtypes = [V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
         lib.pa_decode_int8_workspace_size.restype = sz
         lib.pa_decode_int8_workspace_size.argtypes = [S, i32]
+        lib.pa_reshape_and_cache_fp8.restype = i32
+        lib.pa_reshape_and_cache_fp8.argtypes = [V, V, V, i64, V, V, S, V]
+        lib.pa_decode_fp8.restype = i32
+        lib.pa_decode_fp8.argtypes = [V, V, V, V, V, f32, V, V, S, i32, V, sz, V]
+        lib.pa_decode_fp8_workspace_size.restype = sz
+        lib.pa_decode_fp8_workspace_size.argtypes = [S, i32]
         lib.pa_decode_cascade.restype = i32
         lib.pa_decode_cascade.argtypes = [V, V, V, V, V, V, i32, V, V, V, i32, i32, i32, f32,
                                           V, V, S, V, sz, V]
@@ -172,19 +181,19 @@ def make_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_bl
                     int(block_size), int(max_blocks_per_seq), int(num_blocks))
 
 
-# bytes of one (block, KV head) tile of the int8 pool: 16 x 128 codes, then
-# the 16 rows' fp32 scales
+# bytes of one (block, KV head) tile of the int8 and FP8 pools: 16 x 128
+# one-byte codes, then the 16 rows' fp32 scales
 PA_INT8_TILE_BYTES = 2112
 INT8_BLOCK, INT8_HEAD_DIM = 16, 128
 
 
 def shape_of(q, k_cache, block_tables, num_seqs=None) -> pa_shape:
     """Shape struct from the tensors: q [*, Hq, D], k_cache [NB, Hkv, BS, D]
-    (bf16) or [NB, Hkv, PA_INT8_TILE_BYTES] (uint8, the int8 pool),
+    (bf16) or [NB, Hkv, PA_INT8_TILE_BYTES] (uint8, the int8 or FP8 pool),
     block_tables [S, max_blocks]."""
     if k_cache.dim() == 3 and k_cache.dtype == torch.uint8:
         if k_cache.shape[2] != PA_INT8_TILE_BYTES:
-            raise ValueError(f"int8 pool tiles must be {PA_INT8_TILE_BYTES} bytes")
+            raise ValueError(f"8-bit pool tiles must be {PA_INT8_TILE_BYTES} bytes")
         NB, Hkv = k_cache.shape[:2]
         BS, D = INT8_BLOCK, INT8_HEAD_DIM
     else:
@@ -241,9 +250,7 @@ def pa_decode_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
     return int(load().pa_decode_workspace_size(ctypes.byref(shape), int(num_splits)))
 
 
-def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
-    """Quantising cache write into the int8 pool (uint8 tiles [NB, Hkv, 2112]:
-    a tile's 16 x 128 codes, then its 16 fp32 row scales)."""
+def _cache_write_q8(name, k, v, slot_mapping, k_cache, v_cache, stream):
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
     _need(slot_mapping, "slot_mapping", torch.int64, 1)
@@ -256,10 +263,20 @@ def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, stream=None)
     sh = shape_of(k, k_cache, torch.empty((0, 0)))
     if k.shape[1:] != (sh.num_kv_heads, sh.head_dim):
         raise ValueError("k rows do not match the cache")
-    _check(load().pa_reshape_and_cache_int8(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
-                                            _ptr(k_cache), _ptr(v_cache), ctypes.byref(sh),
-                                            _stream(stream)),
-           "pa_reshape_and_cache_int8")
+    _check(getattr(load(), name)(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0],
+                                 _ptr(k_cache), _ptr(v_cache), ctypes.byref(sh),
+                                 _stream(stream)), name)
+
+
+def pa_reshape_and_cache_int8(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Quantising cache write into the int8 pool (uint8 tiles [NB, Hkv, 2112]:
+    a tile's 16 x 128 codes, then its 16 fp32 row scales)."""
+    _cache_write_q8("pa_reshape_and_cache_int8", k, v, slot_mapping, k_cache, v_cache, stream)
+
+
+def pa_reshape_and_cache_fp8(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Quantising cache write into the FP8 (E4M3) pool (same tiles as int8)."""
+    _cache_write_q8("pa_reshape_and_cache_fp8", k, v, slot_mapping, k_cache, v_cache, stream)
 
 
 def pa_decode_cascade_workspace_size(shape: pa_shape, num_groups: int, num_members: int,
@@ -313,9 +330,12 @@ def pa_decode_int8_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
     return int(load().pa_decode_int8_workspace_size(ctypes.byref(shape), int(num_splits)))
 
 
-def pa_decode_int8(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
-                   num_splits: int = 0, workspace=None, stream=None) -> None:
-    """Decode over the int8 pool with the dequantisation fused."""
+def pa_decode_fp8_workspace_size(shape: pa_shape, num_splits: int = 0) -> int:
+    return int(load().pa_decode_fp8_workspace_size(ctypes.byref(shape), int(num_splits)))
+
+
+def _decode_q8(name, q, k_cache, v_cache, block_tables, context_lens, scale, out, lse,
+               num_splits, workspace, stream):
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.uint8, 3)
     _need(v_cache, "v_cache", torch.uint8, 3)
@@ -332,11 +352,24 @@ def pa_decode_int8(q, k_cache, v_cache, block_tables, context_lens, scale, out, 
     if out.shape != q.shape:
         raise ValueError("out shape != q shape")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().pa_decode_int8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+    _check(getattr(load(), name)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                  _ptr(context_lens), float(scale), _ptr(out), _ptr(lse),
                                  ctypes.byref(sh), int(num_splits), _ptr(workspace), ws_bytes,
-                                 _stream(stream)),
-           "pa_decode_int8")
+                                 _stream(stream)), name)
+
+
+def pa_decode_int8(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
+                   num_splits: int = 0, workspace=None, stream=None) -> None:
+    """Decode over the int8 pool with the dequantisation fused."""
+    _decode_q8("pa_decode_int8", q, k_cache, v_cache, block_tables, context_lens, scale, out,
+               lse, num_splits, workspace, stream)
+
+
+def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, out, lse=None,
+                  num_splits: int = 0, workspace=None, stream=None) -> None:
+    """Decode over the FP8 (E4M3) pool with the dequantisation fused."""
+    _decode_q8("pa_decode_fp8", q, k_cache, v_cache, block_tables, context_lens, scale, out,
+               lse, num_splits, workspace, stream)
 
 
 def _prepared(cfn, args, stream, what, keep):

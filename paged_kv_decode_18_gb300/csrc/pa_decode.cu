@@ -43,24 +43,28 @@ namespace {
 constexpr int kG = 2;                          // query heads per KV head (built)
 constexpr int kQBytes = kG * kHeadDim * 2;     // 512
 
+// Pool element formats of the decode kernel.
+enum : int { kFmtBf16 = 0, kFmtI8 = 1, kFmtF8 = 2 };
+
 // Stage layout for a KV element format: the K tile, the V tile, then q (at a
 // piece's first tile). A tile is one bulk copy of the pool's (block, KV head)
-// run: bf16 [16][128] (4 KB), or int8 codes [16][128] (2 KB) followed by the
-// 16 rows' fp32 scales.
-template <bool Q8>
+// run: bf16 [16][128] (4 KB), or 8-bit codes (int8 or FP8 E4M3) [16][128]
+// (2 KB) followed by the 16 rows' fp32 scales.
+template <int FMT>
 struct KvFormat {
+  static constexpr bool Q8 = FMT != kFmtBf16;  // one-byte codes with row scales
   static constexpr int kTile = Q8 ? kInt8TileBytes : kTileBytes;  // one K or V tile, bytes
   static constexpr int kRow = Q8 ? kHeadDim : 2 * kHeadDim;      // one token row's values, bytes
-  static constexpr int kScaleOff = kBlock * kHeadDim;            // int8: scales within a tile
+  static constexpr int kScaleOff = kBlock * kHeadDim;            // 8-bit: scales within a tile
   static constexpr int kQOff = 2 * kTile;
   static constexpr int kStage = kQOff + kQBytes;
   static_assert(kTile % 16 == 0 && kStage % 16 == 0, "bulk copies need 16-byte alignment");
-  static_assert(!Q8 || kScaleOff + kBlock * 4 == kTile, "int8 scales end the tile");
+  static_assert(!Q8 || kScaleOff + kBlock * 4 == kTile, "8-bit row scales end the tile");
 };
 
-template <int NSTAGE, bool Q8>
+template <int NSTAGE, int FMT>
 struct WarpLayout {
-  static constexpr int kStageBytes = KvFormat<Q8>::kStage;
+  static constexpr int kStageBytes = KvFormat<FMT>::kStage;
   static constexpr int kBarOff = NSTAGE * kStageBytes;
   static constexpr int kPOff = kBarOff + ((NSTAGE * 8 + 15) / 16) * 16;
   static constexpr int kBytes = ((kPOff + 128 + 127) / 128) * 128;
@@ -70,7 +74,7 @@ enum : int { kBalanced = 0, kFixed = 1 };
 
 struct DecodeArgs {
   const uint16_t* q;
-  const unsigned char* k_cache;  // bf16 or int8 tiles (KvFormat)
+  const unsigned char* k_cache;  // bf16, int8 or FP8 tiles (KvFormat)
   const unsigned char* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
@@ -222,10 +226,31 @@ __device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& lo, float2& hi) {
                   bias);
 }
 
+// Two FP8 E4M3 codes (low byte first) -> a float pair, exactly: the hardware
+// conversion to a half pair (every E4M3 value is a normal half), then widening.
+// The NaN codes 0x7F / 0xFF become NaN.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t w16) {
+  float2 f;
+  asm("{\n\t.reg .b16 c, lo, hi;\n\t.reg .b32 h2;\n\t"
+      "cvt.u16.u32 c, %2;\n\tcvt.rn.f16x2.e4m3x2 h2, c;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(w16));
+  return f;
+}
+
 // The 16 dims 16*c8 .. 16*c8+15 of one token row in stage memory, as 8 pairs.
-template <bool Q8>
+template <int FMT>
 __device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)[8]) {
-  if constexpr (Q8) {
+  if constexpr (FMT == kFmtF8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row);
+    const uint32_t wk[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = e4m3x2_to_f2(wk[j] & 0xffffu);
+      f[2 * j + 1] = e4m3x2_to_f2(wk[j] >> 16);
+    }
+  } else if constexpr (FMT == kFmtI8) {
     const uint4 w = *reinterpret_cast<const uint4*>(row);
     i8x4_to_f2(w.x, f[0], f[1]);
     i8x4_to_f2(w.y, f[2], f[3]);
@@ -240,11 +265,12 @@ __device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)
   }
 }
 
-template <int NWARPS, int NSTAGE, bool Q8>
-__global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
+template <int NWARPS, int NSTAGE, int FMT>
+__global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 2 : 1)
     paged_decode_kernel(const DecodeArgs a) {
-  using L = WarpLayout<NSTAGE, Q8>;
-  using F = KvFormat<Q8>;
+  using L = WarpLayout<NSTAGE, FMT>;
+  using F = KvFormat<FMT>;
+  constexpr bool Q8 = F::Q8;
   constexpr int kStageBytes = F::kStage;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -472,7 +498,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float2 kf[8];
-      load_row16<Q8>(Ks + i * F::kRow, kf);
+      load_row16<FMT>(Ks + i * F::kRow, kf);
       float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -496,7 +522,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
       }
     }
     const int tok = grp * 4 + ((lane & 7) >> 1);
-    // int8: the row's K scale multiplies its dot product
+    // 8-bit codes: the row's K scale multiplies its dot product
     float s_val = sc[0];
     if constexpr (Q8) s_val *= reinterpret_cast<const float*>(st + F::kScaleOff)[tok];
     s_val = tok < nvalid ? s_val : neg_inf();
@@ -535,12 +561,12 @@ __global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
     const unsigned char* Vs = st + F::kTile + grp * 4 * F::kRow + c8 * (F::kRow / 8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      if constexpr (Q8) {
+      if constexpr (FMT == kFmtI8) {
         // int8 codes are always finite, so a row past the context needs no
         // skip: its weight is 0 and its V scale (which may hold anything) is
         // replaced by 0. The row's V scale folds into its weights.
         float2 vf[8];
-        load_row16<Q8>(Vs + i * F::kRow, vf);
+        load_row16<FMT>(Vs + i * F::kRow, vf);
         const float vs =
             reinterpret_cast<const float*>(st + F::kTile + F::kScaleOff)[grp * 4 + i];
         const float vsc = grp * 4 + i < nvalid ? vs : 0.f;
@@ -552,12 +578,19 @@ __global__ void __launch_bounds__(NWARPS * 32, Q8 || NWARPS <= 6 ? 2 : 1)
           acc[1][j] = __ffma2_rn(p1, vf[j], acc[1][j]);
         }
       } else if (nvalid == kBlock || grp * 4 + i < nvalid) {
-        // bf16 tokens past the context may hold anything (even NaN): skip,
-        // never 0*x
+        // bf16 and FP8 tokens past the context may hold anything (even NaN):
+        // skip, never 0*x. FP8: the row's V scale folds into its weights.
         float2 vf[8];
-        load_row16<Q8>(Vs + i * F::kRow, vf);
-        const float2 p0 = make_float2(pv[2 * i], pv[2 * i]);
-        const float2 p1 = make_float2(pv[2 * i + 1], pv[2 * i + 1]);
+        load_row16<FMT>(Vs + i * F::kRow, vf);
+        float w0 = pv[2 * i], w1 = pv[2 * i + 1];
+        if constexpr (FMT == kFmtF8) {
+          const float vs =
+              reinterpret_cast<const float*>(st + F::kTile + F::kScaleOff)[grp * 4 + i];
+          w0 *= vs;
+          w1 *= vs;
+        }
+        const float2 p0 = make_float2(w0, w0);
+        const float2 p1 = make_float2(w1, w1);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           acc[0][j] = __ffma2_rn(p0, vf[j], acc[0][j]);
@@ -851,6 +884,7 @@ constexpr int kStages = 2;    // bf16: 2 x 8 KB of copies in flight per warp
 // codes and scales), two CTAs per SM. The int8 loop is bound by instruction
 // issue (the dequantising conversions), not by copies in flight: a sweep of
 // 4-8 warps x 2-3 stages put this shape level with the best on every batch.
+// FP8 pools share the int8 tile and shape.
 constexpr int kWarpsQ8 = 6;
 constexpr int kStagesQ8 = 2;
 
@@ -871,11 +905,11 @@ struct DecodeGeometry {
   int nstages = kStages;  // stages per warp
 };
 
-// A CTA shape of the decode grid: NW warps of NST stages, pool format Q8.
-template <bool Q8, int NW, int NST>
+// A CTA shape of the decode grid: NW warps of NST stages, pool format FMT.
+template <int FMT, int NW, int NST>
 struct DecodeShape {
   static cudaError_t launch(const DecodeGeometry& g, const DecodeArgs& a, cudaStream_t st) {
-    return launch_dependent(paged_decode_kernel<NW, NST, Q8>, dim3(g.grid), dim3(NW * 32), g.smem,
+    return launch_dependent(paged_decode_kernel<NW, NST, FMT>, dim3(g.grid), dim3(NW * 32), g.smem,
                             st, a);
   }
 };
@@ -890,18 +924,18 @@ inline size_t plan_smem_bytes(int S, int parts = 1) {
 // num_splits 0: balanced cut of the sequences' tiles; P >= 2: balanced cut of
 // the tiles of P partitions per sequence when their plan fits in shared
 // memory (the kFixed layout of one warp per partition otherwise); 1: kFixed.
-template <bool Q8, int NW, int NST>
+template <int FMT, int NW, int NST>
 int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int max_sms = 0) {
   constexpr int kWarps = NW;
   g->nwarps = NW;
   g->nstages = NST;
-  g->launch = &DecodeShape<Q8, NW, NST>::launch;
+  g->launch = &DecodeShape<FMT, NW, NST>::launch;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const int S = sh->num_seqs, Hkv = sh->num_kv_heads, Hq = sh->num_q_heads;
-  const void* kern = reinterpret_cast<const void*>(paged_decode_kernel<NW, NST, Q8>);
+  const void* kern = reinterpret_cast<const void*>(paged_decode_kernel<NW, NST, FMT>);
   if (!raise_smem_limit(kern)) return PA_ERR_CUDA;
-  const size_t warp_bytes = (size_t)kWarps * WarpLayout<NST, Q8>::kBytes;
+  const size_t warp_bytes = (size_t)kWarps * WarpLayout<NST, FMT>::kBytes;
   const int parts = num_splits >= 2 ? num_splits : 1;
   if (num_splits != 1 && warp_bytes + plan_smem_bytes(S, parts) <= (size_t)dev.max_smem_optin) {
     g->smem = warp_bytes + plan_smem_bytes(S, parts);
@@ -942,15 +976,18 @@ int decode_geometry_t(const pa_shape* sh, int num_splits, DecodeGeometry* g, int
   return PA_OK;
 }
 
-int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, bool q8 = false,
+int decode_geometry(const pa_shape* sh, int num_splits, DecodeGeometry* g, int fmt = kFmtBf16,
                     int max_sms = 0) {
-  if (q8) return decode_geometry_t<true, kWarpsQ8, kStagesQ8>(sh, num_splits, g, max_sms);
+  if (fmt == kFmtI8)
+    return decode_geometry_t<kFmtI8, kWarpsQ8, kStagesQ8>(sh, num_splits, g, max_sms);
+  if (fmt == kFmtF8)
+    return decode_geometry_t<kFmtF8, kWarpsQ8, kStagesQ8>(sh, num_splits, g, max_sms);
   DeviceInfo dev;
   if (!current_device_info(&dev)) return PA_ERR_CUDA;
   const bool long_ctx = num_splits != 1 && max_sms == 0 &&
                         (int64_t)sh->num_seqs * sh->num_kv_heads <= dev.num_sms;
-  return long_ctx ? decode_geometry_t<false, kWarpsLong, kStages>(sh, num_splits, g, max_sms)
-                  : decode_geometry_t<false, kWarps, kStages>(sh, num_splits, g, max_sms);
+  return long_ctx ? decode_geometry_t<kFmtBf16, kWarpsLong, kStages>(sh, num_splits, g, max_sms)
+                  : decode_geometry_t<kFmtBf16, kWarps, kStages>(sh, num_splits, g, max_sms);
 }
 
 int check_decode_args(const pa_shape* shape, int num_splits) {
@@ -993,7 +1030,15 @@ extern "C" size_t pa_decode_int8_workspace_size(const pa_shape* shape, int num_s
   if (check_decode_args(shape, num_splits) != PA_OK) return 0;
   if (shape->num_seqs == 0) return 0;
   DecodeGeometry g;
-  if (decode_geometry(shape, num_splits, &g, true) != PA_OK) return 0;
+  if (decode_geometry(shape, num_splits, &g, kFmtI8) != PA_OK) return 0;
+  return g.ws_bytes;
+}
+
+extern "C" size_t pa_decode_fp8_workspace_size(const pa_shape* shape, int num_splits) {
+  if (check_decode_args(shape, num_splits) != PA_OK) return 0;
+  if (shape->num_seqs == 0) return 0;
+  DecodeGeometry g;
+  if (decode_geometry(shape, num_splits, &g, kFmtF8) != PA_OK) return 0;
   return g.ws_bytes;
 }
 
@@ -1006,8 +1051,8 @@ thread_local int g_inject_missing_copy = -1;
 
 // Validate, size and launch the decode grid and its merge. `early`: see the
 // kernel (only pa_append_decode sets it).
-// q8 selects the int8 pool format.
-int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache, bool q8,
+// fmt selects the pool format (bf16, int8 or FP8 tiles).
+int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache, int fmt,
                 const int32_t* block_tables, const int32_t* context_lens, float scale,
                 pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
                 void* workspace, size_t workspace_bytes, cudaStream_t st, int early,
@@ -1022,7 +1067,7 @@ int decode_impl(const pa_bf16* q, const void* k_cache, const void* v_cache, bool
     return PA_ERR_ARG;
   if (!(scale == scale)) return PA_ERR_ARG;
   DecodeGeometry g;
-  rc = decode_geometry(shape, num_splits, &g, q8, max_sms);
+  rc = decode_geometry(shape, num_splits, &g, fmt, max_sms);
   if (rc != PA_OK) return rc;
   if (g.ws_bytes > 0 &&
       (!workspace || workspace_bytes < g.ws_bytes || !aligned(workspace, 256)))
@@ -1115,7 +1160,7 @@ int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
                 const int32_t* block_tables, const int32_t* context_lens, float scale,
                 const pa_shape* shape, const RowsOut& rows, void* workspace,
                 size_t workspace_bytes, cudaStream_t st, int late, int max_sms) {
-  return decode_impl(q, k_cache, v_cache, false, block_tables, context_lens, scale,
+  return decode_impl(q, k_cache, v_cache, kFmtBf16, block_tables, context_lens, scale,
                      nullptr, nullptr, shape, 0, workspace, workspace_bytes, st, 0, &rows, late,
                      max_sms);
 }
@@ -1123,7 +1168,7 @@ int decode_rows(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16* v_cache
 size_t decode_rows_workspace_size(const pa_shape* shape, int max_sms) {
   if (check_decode_args(shape, 0) != PA_OK || shape->num_seqs == 0) return 0;
   DecodeGeometry g;
-  if (decode_geometry(shape, 0, &g, false, max_sms) != PA_OK) return 0;
+  if (decode_geometry(shape, 0, &g, kFmtBf16, max_sms) != PA_OK) return 0;
   return g.ws_bytes;
 }
 
@@ -1134,7 +1179,7 @@ extern "C" int pa_decode(const pa_bf16* q, const pa_bf16* k_cache, const pa_bf16
                          pa_bf16* out, float* lse, const pa_shape* shape, int num_splits,
                          void* workspace, size_t workspace_bytes, void* stream) {
   pa::NvtxRange nvtx_range("pa_decode");
-  return decode_impl(q, k_cache, v_cache, false, block_tables, context_lens, scale,
+  return decode_impl(q, k_cache, v_cache, kFmtBf16, block_tables, context_lens, scale,
                      out, lse, shape, num_splits, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), 0);
 }
@@ -1145,7 +1190,18 @@ extern "C" int pa_decode_int8(const pa_bf16* q, const uint8_t* k_cache, const ui
                               int num_splits, void* workspace, size_t workspace_bytes,
                               void* stream) {
   pa::NvtxRange nvtx_range("pa_decode_int8");
-  return decode_impl(q, k_cache, v_cache, true, block_tables, context_lens, scale, out, lse,
+  return decode_impl(q, k_cache, v_cache, kFmtI8, block_tables, context_lens, scale, out, lse,
+                     shape, num_splits, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), 0);
+}
+
+extern "C" int pa_decode_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             float scale, pa_bf16* out, float* lse, const pa_shape* shape,
+                             int num_splits, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  pa::NvtxRange nvtx_range("pa_decode_fp8");
+  return decode_impl(q, k_cache, v_cache, kFmtF8, block_tables, context_lens, scale, out, lse,
                      shape, num_splits, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), 0);
 }
@@ -1179,7 +1235,7 @@ extern "C" int pa_append_decode(const pa_bf16* k_new, const pa_bf16* v_new,
   // with new tokens, the cache write ran just before: the decode prologue
   // (which reads only context_lens and block_tables) and every tile but the
   // segments' last ones may overlap it
-  return decode_impl(q, k_cache, v_cache, false, block_tables, context_lens, scale,
+  return decode_impl(q, k_cache, v_cache, kFmtBf16, block_tables, context_lens, scale,
                      out, lse, shape, 0, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), num_new_tokens > 0 ? 1 : 0);
 }

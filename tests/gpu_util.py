@@ -79,35 +79,43 @@ def int8_pools_numpy(kc, vc):
 
 
 class Int8Batch:
-    """A workload on the GPU with its int8 pool written by the CUDA quantising
-    cache write (history first, then the step's new tokens)."""
+    """A workload on the GPU with its 8-bit pool (int8, or FP8 E4M3 with
+    fp8=True) written by the CUDA quantising cache write (history first, then
+    the step's new tokens)."""
 
-    def __init__(self, w):
+    def __init__(self, w, fp8=False):
         dev = device()
-        self.w, self.dev = w, dev
-        self.kc, self.vc = w.empty_pool_i8(dev)
+        self.w, self.dev, self.fp8 = w, dev, fp8
+        self.kc, self.vc = w.empty_pool_f8(dev) if fp8 else w.empty_pool_i8(dev)
+        write = B.pa_reshape_and_cache_fp8 if fp8 else B.pa_reshape_and_cache_int8
         if w.k_hist.shape[0]:
-            B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                        self.kc, self.vc)
-        B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev),
-                                    self.kc, self.vc)
+            write(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), self.kc, self.vc)
+        write(w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev), self.kc, self.vc)
         self.q = w.q.to(dev)
         self.bt = w.block_tables.to(dev)
         self.cl = w.context_lens.to(dev)
 
     def pools(self):
         """(k codes, v codes, k scales, v scales) as numpy, split out of the
-        tile layout."""
-        return int8_pools_numpy(self.kc, self.vc)
+        tile layout (FP8 codes as uint8)."""
+        kc, vc, ks, vs = int8_pools_numpy(self.kc, self.vc)
+        if self.fp8:
+            kc, vc = kc.view(np.uint8), vc.view(np.uint8)
+        return kc, vc, ks, vs
 
     def decode(self, num_splits=0, with_lse=True):
         out = torch.empty_like(self.q)
         lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=self.dev) \
             if with_lse else None
         sh = B.shape_of(self.q, self.kc, self.bt)
-        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, num_splits), self.dev)
-        B.pa_decode_int8(self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale, out, lse,
-                         num_splits=num_splits, workspace=ws)
+        if self.fp8:
+            ws = B.workspace(B.pa_decode_fp8_workspace_size(sh, num_splits), self.dev)
+            B.pa_decode_fp8(self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale, out, lse,
+                            num_splits=num_splits, workspace=ws)
+        else:
+            ws = B.workspace(B.pa_decode_int8_workspace_size(sh, num_splits), self.dev)
+            B.pa_decode_int8(self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale, out, lse,
+                             num_splits=num_splits, workspace=ws)
         return out, lse
 
 
