@@ -848,17 +848,20 @@ def run_case(args, dev):
         w = W.mixed(seed=args.seed, num_verify=0)
     elif args.case == "prefill_long":  # two 2048-token chunks (contexts 2048 and 8192)
         w = W.mixed(seed=args.seed, num_verify=0, prefill_chunk=2048, prefill_offsets=(0, 6144))
-    elif args.case in ("ragged_int8", "engine_int8", "long_int8"):
-        w = W.make(args.case[:-5], seed=args.seed)
+    elif args.case.endswith(("_int8", "_fp8")):
+        w = W.make(args.case.rsplit("_", 1)[0], seed=args.seed)
     elif args.case == "shared_prompt":
         w = W.shared_prompt(seed=args.seed)
     else:
         w = W.make(args.case, seed=args.seed)
-    int8 = args.case.endswith("_int8")
+    int8 = args.case.endswith(("_int8", "_fp8"))
+    fp8 = args.case.endswith("_fp8")
+    q8_write = B.pa_reshape_and_cache_fp8 if fp8 else B.pa_reshape_and_cache_int8
+    q8_decode = B.pa_decode_fp8 if fp8 else B.pa_decode_int8
+    q8_ws = B.pa_decode_fp8_workspace_size if fp8 else B.pa_decode_int8_workspace_size
     if int8:
-        kc, vc = w.empty_pool_i8(dev)
-        B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                    kc, vc)
+        kc, vc = w.empty_pool_f8(dev) if fp8 else w.empty_pool_i8(dev)
+        q8_write(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
     else:
         kc, vc = w.empty_pool(dev)
         B.pa_reshape_and_cache(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
@@ -873,7 +876,7 @@ def run_case(args, dev):
     if varlen:
         ws = B.workspace(B.pa_decode_varlen_workspace_size(sh, q.shape[0], w.max_q_len), dev)
     elif int8:
-        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, args.splits), dev)
+        ws = B.workspace(q8_ws(sh, args.splits), dev)
     elif cascade:
         sg, cg, mem, pl, mg, mp = W.cascade_groups(w)
         sg, cg, mem, pl = sg.to(dev), cg.to(dev), mem.to(dev), pl.to(dev)
@@ -884,9 +887,9 @@ def run_case(args, dev):
 
     def step():
         if int8:
-            B.pa_reshape_and_cache_int8(k_new, v_new, slot_new, kc, vc)
-            B.pa_decode_int8(q, kc, vc, bt, cl, w.scale, out, lse,
-                             num_splits=args.splits, workspace=ws)
+            q8_write(k_new, v_new, slot_new, kc, vc)
+            q8_decode(q, kc, vc, bt, cl, w.scale, out, lse, num_splits=args.splits,
+                      workspace=ws)
             return
         B.pa_reshape_and_cache(k_new, v_new, slot_new, kc, vc)
         if varlen:
@@ -960,6 +963,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["tiny", "engine", "ragged", "long", "mixed", "prefill", "prefill_long",
                                        "ragged_int8", "engine_int8", "long_int8",
+                                       "ragged_fp8", "engine_fp8", "long_fp8",
                                        "shared_prompt"],
                     help="time one workload with eager calls (for profiling), nothing else")
     ap.add_argument("--splits", type=int, default=0, help="num_splits for --case decode runs")

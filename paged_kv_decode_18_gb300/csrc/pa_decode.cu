@@ -29,11 +29,16 @@
 // A batch is cut into equal tile ranges over all resident warps (num_splits
 // 0), so ragged batches and long contexts balance; a (sequence, KV head) cut
 // by a range boundary leaves partials that a small merge kernel combines.
-// The same kernel, templated on the pool format, serves the INT8 pool (one
-// fp32 scale per (token, KV head) row): the codes become fp32 exactly (a byte
-// permute into the mantissa of 2^23 and one packed subtraction) before the
-// same products, and the row scales fold into the dot product and the softmax
-// weight.
+// The same kernel, templated on the pool format, serves the 8-bit pools
+// (int8 or FP8 E4M3 codes, one fp32 scale per (token, KV head) row). There
+// the per-value conversions plus fp32 products made the loop issue-bound, so
+// both contractions of a tile run on warp MMAs instead (m16n8k16, f16
+// operands, fp32 accumulation): the codes become f16 exactly (the hardware
+// E4M3 conversion; for int8 a byte permute into the mantissa of the half 1024
+// and one packed subtraction), q is scaled by a power of two so it is exact
+// in f16, the K row scales multiply the scores, and the V row scales fold
+// into the softmax weights (normalised per tile so they fit f16). The integer
+// MMA (s8) was measured 1.8x slower on this part: its int8 tensor rate is low.
 #include "pa_device.cuh"
 #include "pa_host.h"
 
@@ -54,7 +59,6 @@ template <int FMT>
 struct KvFormat {
   static constexpr bool Q8 = FMT != kFmtBf16;  // one-byte codes with row scales
   static constexpr int kTile = Q8 ? kInt8TileBytes : kTileBytes;  // one K or V tile, bytes
-  static constexpr int kRow = Q8 ? kHeadDim : 2 * kHeadDim;      // one token row's values, bytes
   static constexpr int kScaleOff = kBlock * kHeadDim;            // 8-bit: scales within a tile
   static constexpr int kQOff = 2 * kTile;
   static constexpr int kStage = kQOff + kQBytes;
@@ -213,56 +217,57 @@ __device__ __forceinline__ void merge_segment(const MergeJob& job, int w, int la
   }
 }
 
-// Four signed bytes -> two float pairs, exactly: the byte (biased by 128)
-// becomes the low mantissa bits of 2^23, one packed subtraction removes both.
-__device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& lo, float2& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  const float2 bias = make_float2(-8388736.f, -8388736.f);  // 2^23 + 128
-  lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                              __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
-                  bias);
-  hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                              __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
-                  bias);
-}
-
-// Two FP8 E4M3 codes (low byte first) -> a float pair, exactly: the hardware
-// conversion to a half pair (every E4M3 value is a normal half), then widening.
-// The NaN codes 0x7F / 0xFF become NaN.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t w16) {
-  float2 f;
-  asm("{\n\t.reg .b16 c, lo, hi;\n\t.reg .b32 h2;\n\t"
-      "cvt.u16.u32 c, %2;\n\tcvt.rn.f16x2.e4m3x2 h2, c;\n\t"
-      "mov.b32 {lo, hi}, h2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-      : "=f"(f.x), "=f"(f.y)
-      : "r"(w16));
-  return f;
-}
-
-// The 16 dims 16*c8 .. 16*c8+15 of one token row in stage memory, as 8 pairs.
-template <int FMT>
+// The 16 dims 16*c8 .. 16*c8+15 of one bf16 token row in stage memory, as 8 pairs.
 __device__ __forceinline__ void load_row16(const unsigned char* row, float2 (&f)[8]) {
+  const uint4 wa = *reinterpret_cast<const uint4*>(row);
+  const uint4 wb = *reinterpret_cast<const uint4*>(row + 16);
+  const uint32_t wk[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = make_float2(bf_lo(wk[j]), bf_hi(wk[j]));
+}
+
+// Two floats -> an f16 pair (lo in the low half), rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Four 8-bit codes (bytes 0..3 of w) -> two f16 pairs, exactly: (byte 0, 1)
+// in lo, (byte 2, 3) in hi. FP8 E4M3: the hardware conversion (every E4M3
+// value is a normal half; the NaN codes become NaN). int8: the byte, biased
+// by 128, becomes the low mantissa bits of the half 1024; one packed
+// subtraction of 1152 leaves the code.
+template <int FMT>
+__device__ __forceinline__ void codes_to_h2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   if constexpr (FMT == kFmtF8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(row);
-    const uint32_t wk[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = e4m3x2_to_f2(wk[j] & 0xffffu);
-      f[2 * j + 1] = e4m3x2_to_f2(wk[j] >> 16);
-    }
-  } else if constexpr (FMT == kFmtI8) {
-    const uint4 w = *reinterpret_cast<const uint4*>(row);
-    i8x4_to_f2(w.x, f[0], f[1]);
-    i8x4_to_f2(w.y, f[2], f[3]);
-    i8x4_to_f2(w.z, f[4], f[5]);
-    i8x4_to_f2(w.w, f[6], f[7]);
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
   } else {
-    const uint4 wa = *reinterpret_cast<const uint4*>(row);
-    const uint4 wb = *reinterpret_cast<const uint4*>(row + 16);
-    const uint32_t wk[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) f[j] = make_float2(bf_lo(wk[j]), bf_hi(wk[j]));
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t blo = __byte_perm(u, 0x64646464u, 0x4140u);
+    const uint32_t bhi = __byte_perm(u, 0x64646464u, 0x4342u);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(blo), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(bhi), "r"(0x64806480u));
   }
+}
+
+// d += A * B for one m16n8k16 tile: A row-major 16 x 16 f16 (a0: row g, k
+// 2c..2c+1; a1: row g+8, same k; a2: row g, k 2c+8..2c+9; a3: row g+8), B
+// 16 x 8 f16 (b0: k 2c..2c+1, column g; b1: k 2c+8..2c+9), fp32 d (d0, d1:
+// row g, columns 2c, 2c+1; d2, d3: row g+8), where g = lane / 4, c = lane % 4.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 template <int NWARPS, int NSTAGE, int FMT>
@@ -449,215 +454,424 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
 
   for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
 
-  // ---- consumer -------------------------------------------------------------
-  // Lane (grp, c8) holds dims 16*c8..16*c8+15 of tokens 4*grp..4*grp+3 for
-  // both query heads; fp32 pairs go through the packed (f32x2) FMA pipe.
-  TilePos cp = locate(P, S, Hkv, R0);
-  float2 q2[kG][8];    // scaled q, dims (16*c8 + 2j, +1)
-  float2 acc[kG][8];   // output accumulator, same dims
-  float m0 = neg_inf(), m1 = neg_inf(), l_lane = 0.f;
-  int piece_b0 = 0;
-  bool piece_first = true;
-
-  int k = 0;
-  for (int idx = R0; idx < R1; ++idx, ++k) {
-    const int stage = k % NSTAGE;
-    const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
-    if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
-      // a copy never landed: give the remaining ones a bounded wait, then stop
-      for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
-        mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
-      late_exit();
-      return;
-    }
-    unsigned char* st = wbuf + stage * kStageBytes;
-    const bool first = (idx == R0) || (cp.b == 0);
-    if (first) {
-#pragma unroll
-      for (int g = 0; g < kG; ++g) {
-        const uint4* qs = reinterpret_cast<const uint4*>(st + F::kQOff + g * 256 + c8 * 32);
-        const uint4 qa = qs[0], qb = qs[1];
-        const uint32_t wq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          q2[g][j] = make_float2(bf_lo(wq[j]) * a.scale_log2, bf_hi(wq[j]) * a.scale_log2);
-          acc[g][j] = make_float2(0.f, 0.f);
-        }
-      }
-      m0 = neg_inf();
-      m1 = neg_inf();
-      l_lane = 0.f;
-      piece_b0 = cp.b;
-      piece_first = (idx == R0);
-    }
-    const int nvalid = min(kBlock, P.ctx[cp.s] - abs_block(cp) * kBlock);
-
-    // ---- scores: 4 tokens x 2 heads of partial dots per lane ----------------
-    float sc[8];
-    const unsigned char* Ks = st + grp * 4 * F::kRow + c8 * (F::kRow / 8);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 kf[8];
-      load_row16<FMT>(Ks + i * F::kRow, kf);
-      float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        d0 = __ffma2_rn(q2[0][j], kf[j], d0);
-        d1 = __ffma2_rn(q2[1][j], kf[j], d1);
-      }
-      sc[2 * i] = d0.x + d0.y;
-      sc[2 * i + 1] = d1.x + d1.y;
-    }
-    // reduce-scatter over the 8 lanes of this group: value v = 2*i + g ends in
-    // the lane with (lane & 7) == v
-#pragma unroll
-    for (int step = 0; step < 3; ++step) {
-      const int half = 4 >> step;
-      const bool upper = (lane & half) != 0;
-#pragma unroll
-      for (int j = 0; j < half; ++j) {
-        const float send = upper ? sc[j] : sc[j + half];
-        const float keep = upper ? sc[j + half] : sc[j];
-        sc[j] = keep + __shfl_xor_sync(kFull, send, half);
-      }
-    }
-    const int tok = grp * 4 + ((lane & 7) >> 1);
-    // 8-bit codes: the row's K scale multiplies its dot product
-    float s_val = sc[0];
-    if constexpr (Q8) s_val *= reinterpret_cast<const float*>(st + F::kScaleOff)[tok];
-    s_val = tok < nvalid ? s_val : neg_inf();
-
-    // ---- online softmax (log2 domain) ------------------------------------------
-    float mx = s_val;
-#pragma unroll
-    for (int o = 2; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    const float mx_other = __shfl_xor_sync(kFull, mx, 1);
-    const float mn0 = fmaxf(m0, hsel ? mx_other : mx);
-    const float mn1 = fmaxf(m1, hsel ? mx : mx_other);
-    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    const float p = ex2(s_val - (hsel ? mn1 : mn0));
-    l_lane = l_lane * (hsel ? al1 : al0) + p;
+  if constexpr (Q8) {
+    // ---- consumer, 8-bit tiles: the two contractions of a tile on warp MMAs
+    // (m16n8k16, f16 operands, fp32 accumulation). Lane (g, c) = (lane / 4,
+    // lane % 4). Scores: A = the K codes (rows = the tile's 16 tokens) as f16
+    // (exact), B = q scaled by a power of two that puts its largest |q_d| in
+    // [2^14, 2^15) (exact in f16: bf16 has 8 significant bits); column n of B
+    // is head n & 1, so every lane ends with the scores of tokens g and g + 8
+    // for both heads. The contraction order of the dims is free: for MMA j,
+    // the k index pairs (2c, 2c+1) and (2c+8, 2c+9) are dims 32c + 4j + 0..3,
+    // so each lane reads 32 contiguous bytes of rows g and g + 8.
+    // Output: A = the V codes transposed (rows = dims, k = tokens), B = the
+    // softmax weights times each row's V scale, divided by the tile's largest
+    // V scale vmax (so in [0, 1], f16), and the MMA result times vmax joins
+    // the fp32 accumulator. For MMA m, row g is dim 16g + 2m and row g + 8 is
+    // dim 16g + 2m + 1; k pairs (2c, 2c+1) and (2c+8, 2c+9) are tokens 4c ..
+    // 4c+3, so each lane reads 16 contiguous bytes of four token rows.
+    const int g = lane >> 2, c = lane & 3;
+    const int hq = g & 1;  // the head of B column g
+    TilePos cp = locate(P, S, Hkv, R0);
+    uint32_t qb[16];       // score B fragments: scaled q of head hq, f16 pairs
+    float cq0 = 0.f, cq1 = 0.f;  // per head: scale_log2 / (power-of-two q scale)
+    float acc[8][4];       // output accumulator, MMA C layout (see the finish)
+    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+    int piece_b0 = 0;
+    bool piece_first = true;
     float* pbuf = reinterpret_cast<float*>(wbuf + L::kPOff);
-    pbuf[lane] = p;  // index 2*token + head
-    __syncwarp();
-    float pv[8];
-    {
-      const float4* pb = reinterpret_cast<const float4*>(pbuf + grp * 8);
-      const float4 p0 = pb[0], p1 = pb[1];
-      pv[0] = p0.x; pv[1] = p0.y; pv[2] = p0.z; pv[3] = p0.w;
-      pv[4] = p1.x; pv[5] = p1.y; pv[6] = p1.z; pv[7] = p1.w;
-    }
-    if (al0 != 1.f || al1 != 1.f) {
-      const float2 a0 = make_float2(al0, al0), a1 = make_float2(al1, al1);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc[0][j] = __fmul2_rn(acc[0][j], a0);
-        acc[1][j] = __fmul2_rn(acc[1][j], a1);
+
+    int k = 0;
+    for (int idx = R0; idx < R1; ++idx, ++k) {
+      const int stage = k % NSTAGE;
+      const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
+      if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
+        for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
+          mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
+        late_exit();
+        return;
       }
-    }
-    // ---- PV ----------------------------------------------------------------------
-    const unsigned char* Vs = st + F::kTile + grp * 4 * F::kRow + c8 * (F::kRow / 8);
+      unsigned char* st = wbuf + stage * kStageBytes;
+      const bool first = (idx == R0) || (cp.b == 0);
+      if (first) {
+        const uint4* qs = reinterpret_cast<const uint4*>(st + F::kQOff + hq * 256 + c * 64);
+        float qv[32];
+        float mx = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if constexpr (FMT == kFmtI8) {
-        // int8 codes are always finite, so a row past the context needs no
-        // skip: its weight is 0 and its V scale (which may hold anything) is
-        // replaced by 0. The row's V scale folds into its weights.
-        float2 vf[8];
-        load_row16<FMT>(Vs + i * F::kRow, vf);
-        const float vs =
-            reinterpret_cast<const float*>(st + F::kTile + F::kScaleOff)[grp * 4 + i];
-        const float vsc = grp * 4 + i < nvalid ? vs : 0.f;
-        const float2 p0 = make_float2(pv[2 * i] * vsc, pv[2 * i] * vsc);
-        const float2 p1 = make_float2(pv[2 * i + 1] * vsc, pv[2 * i + 1] * vsc);
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = qs[i];
+          const uint32_t wq[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            qv[8 * i + 2 * j] = bf_lo(wq[j]);
+            qv[8 * i + 2 * j + 1] = bf_hi(wq[j]);
+            mx = fmaxf(mx, fmaxf(fabsf(qv[8 * i + 2 * j]), fabsf(qv[8 * i + 2 * j + 1])));
+          }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        // 2^(141 - e) for |q| max in [2^(e-127), 2^(e-126)); e >= 14 keeps it finite
+        const int e = max((int)((__float_as_uint(mx) >> 23) & 0xffu), 14);
+        const float qsc = __uint_as_float((uint32_t)(268 - e) << 23);
+        const float cq = __fdiv_rn(a.scale_log2, qsc);
+        const float cq_o = __shfl_xor_sync(kFull, cq, 4);  // lane g ^ 1: the other head
+        cq0 = hq ? cq_o : cq;
+        cq1 = hq ? cq : cq_o;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          acc[0][j] = __ffma2_rn(p0, vf[j], acc[0][j]);
-          acc[1][j] = __ffma2_rn(p1, vf[j], acc[1][j]);
+          qb[2 * j] = pack_h2(qv[4 * j] * qsc, qv[4 * j + 1] * qsc);
+          qb[2 * j + 1] = pack_h2(qv[4 * j + 2] * qsc, qv[4 * j + 3] * qsc);
         }
-      } else if (nvalid == kBlock || grp * 4 + i < nvalid) {
-        // bf16 and FP8 tokens past the context may hold anything (even NaN):
-        // skip, never 0*x. FP8: the row's V scale folds into its weights.
-        float2 vf[8];
-        load_row16<FMT>(Vs + i * F::kRow, vf);
-        float w0 = pv[2 * i], w1 = pv[2 * i + 1];
-        if constexpr (FMT == kFmtF8) {
-          const float vs =
-              reinterpret_cast<const float*>(st + F::kTile + F::kScaleOff)[grp * 4 + i];
-          w0 *= vs;
-          w1 *= vs;
-        }
-        const float2 p0 = make_float2(w0, w0);
-        const float2 p1 = make_float2(w1, w1);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+        m0 = neg_inf();
+        m1 = neg_inf();
+        l0 = 0.f;
+        l1 = 0.f;
+        piece_b0 = cp.b;
+        piece_first = (idx == R0);
+      }
+      const int nvalid = min(kBlock, P.ctx[cp.s] - abs_block(cp) * kBlock);
+
+      // ---- scores ---------------------------------------------------------------
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint4* kr0 = reinterpret_cast<const uint4*>(st + g * kHeadDim + c * 32);
+        const uint4* kr1 = reinterpret_cast<const uint4*>(st + (g + 8) * kHeadDim + c * 32);
+        const uint4 x0 = kr0[0], x1 = kr0[1], y0 = kr1[0], y1 = kr1[1];
+        const uint32_t r0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t r1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        float d2[4] = {0.f, 0.f, 0.f, 0.f};  // odd j: a second, independent chain
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          acc[0][j] = __ffma2_rn(p0, vf[j], acc[0][j]);
-          acc[1][j] = __ffma2_rn(p1, vf[j], acc[1][j]);
+          uint32_t a0, a1, a2, a3;
+          codes_to_h2<FMT>(r0[j], a0, a2);
+          codes_to_h2<FMT>(r1[j], a1, a3);
+          if (j & 1)
+            mma_16816(d2, a0, a1, a2, a3, qb[2 * j], qb[2 * j + 1]);
+          else
+            mma_16816(d, a0, a1, a2, a3, qb[2 * j], qb[2 * j + 1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] += d2[i];
+      }
+      const float* ksc = reinterpret_cast<const float*>(st + F::kScaleOff);
+      const float kg0 = ksc[g], kg8 = ksc[g + 8];
+      float s00 = d[0] * cq0 * kg0, s01 = d[1] * cq1 * kg0;  // token g, heads 0 / 1
+      float s10 = d[2] * cq0 * kg8, s11 = d[3] * cq1 * kg8;  // token g + 8
+      if (g >= nvalid) s00 = s01 = neg_inf();
+      if (g + 8 >= nvalid) s10 = s11 = neg_inf();
+
+      // ---- online softmax (log2 domain), per head over the 8 lane groups ---------
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p00 = ex2(s00 - mn0), p01 = ex2(s01 - mn1);
+      const float p10 = ex2(s10 - mn0), p11 = ex2(s11 - mn1);
+      l0 = l0 * al0 + (p00 + p10);
+      l1 = l1 * al1 + (p01 + p11);
+      // weights [head][token] through shared memory to the lanes of B column g
+      if (c < 2) {
+        pbuf[g + 8 * c] = c ? p10 : p00;
+        pbuf[16 + g + 8 * c] = c ? p11 : p01;
+      }
+      __syncwarp();
+      const float4 pw = *reinterpret_cast<const float4*>(pbuf + hq * 16 + 4 * c);
+      const float4 vs4 =
+          *reinterpret_cast<const float4*>(st + F::kTile + F::kScaleOff + 16 * c);
+      // rows past the context may hold anything: their scale counts as 0
+      const float v0 = 4 * c < nvalid ? vs4.x : 0.f, v1 = 4 * c + 1 < nvalid ? vs4.y : 0.f;
+      const float v2 = 4 * c + 2 < nvalid ? vs4.z : 0.f, v3 = 4 * c + 3 < nvalid ? vs4.w : 0.f;
+      float vmax = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 1));
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 2));
+      const float rv = vmax > 0.f ? 1.f / vmax : 0.f;
+      const uint32_t b0 = pack_h2(pw.x * (v0 * rv), pw.y * (v1 * rv));
+      const uint32_t b1 = pack_h2(pw.z * (v2 * rv), pw.w * (v3 * rv));
+
+      // ---- output ------------------------------------------------------------------
+      const unsigned char* Vt = st + F::kTile;
+      uint4 R[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        R[i] = *reinterpret_cast<const uint4*>(Vt + (4 * c + i) * kHeadDim + 16 * g);
+      if constexpr (FMT == kFmtF8) {
+        // E4M3 rows past the context may hold NaN codes: never let them into
+        // the MMA (int8 codes are always finite and meet a zero weight)
+        if (nvalid < kBlock) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (4 * c + i >= nvalid) R[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-    }
-    __syncwarp();  // all lanes are done with this stage's K/V and with pbuf
-    // refill the stage now: finishing a piece below needs no stage memory, so
-    // its work overlaps the copy
-    if (pidx < R1) issue(stage);
+      if (al0 != 1.f || al1 != 1.f) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          acc[m][0] *= al0;
+          acc[m][1] *= al1;
+          acc[m][2] *= al0;
+          acc[m][3] *= al1;
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int wd = m >> 1;
+        // bytes (b, b+1) of each token row's word wd, interleaved by token
+        const uint32_t sel = (m & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x01 = __byte_perm(word_of(R[0], wd), word_of(R[1], wd), sel);
+        const uint32_t x23 = __byte_perm(word_of(R[2], wd), word_of(R[3], wd), sel);
+        uint32_t a0, a1, a2, a3;
+        codes_to_h2<FMT>(x01, a0, a1);
+        codes_to_h2<FMT>(x23, a2, a3);
+        float dv[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(dv, a0, a1, a2, a3, b0, b1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[m][q] = fmaf(vmax, dv[q], acc[m][q]);
+      }
+      __syncwarp();  // all lanes are done with this stage and with pbuf
+      if (pidx < R1) issue(stage);
 
-    const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
-    if (last) {
-      // ---- finish the piece: sum the 4 token groups' accumulators (lanes
-      // c8, c8+8, c8+16, c8+24) by a reduce-scatter over lane bits 4 and 3;
-      // lane (b4, b3, c8) ends with head b4, dims 16*c8 + 8*b3 .. +7 ----------
-      const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
-      float h16[16];  // after lane bit 4: head b4, dims 16*c8 .. 16*c8+15
+      const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
+      if (last) {
+        // ---- finish the piece: acc[m] holds (dim 16g + 2m: head 0, head 1;
+        // dim 16g + 2m + 1: head 0, head 1) in every lane of group g; lane
+        // (g, c) writes head c >> 1, dims 16g + 8 (c & 1) .. +7 -------------------
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float2 mine = b4 ? acc[1][j] : acc[0][j];
-        const float2 send = b4 ? acc[0][j] : acc[1][j];
-        h16[2 * j] = mine.x + __shfl_xor_sync(kFull, send.x, 16);
-        h16[2 * j + 1] = mine.y + __shfl_xor_sync(kFull, send.y, 16);
-      }
-      float o8[8];
+        for (int o = 4; o < 32; o <<= 1) {
+          l0 += __shfl_xor_sync(kFull, l0, o);
+          l1 += __shfl_xor_sync(kFull, l1, o);
+        }
+        const int og = c >> 1;
+        const bool hi = (c & 1) != 0;
+        float o8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float mine = b3 ? h16[8 + i] : h16[i];
-        const float send = b3 ? h16[i] : h16[8 + i];
-        o8[i] = mine + __shfl_xor_sync(kFull, send, 8);
+        for (int i = 0; i < 4; ++i) {
+          const float* lo_m = acc[i];
+          const float* hi_m = acc[4 + i];
+          const float e0 = hi ? hi_m[0] : lo_m[0], e1 = hi ? hi_m[1] : lo_m[1];
+          const float e2 = hi ? hi_m[2] : lo_m[2], e3 = hi ? hi_m[3] : lo_m[3];
+          o8[2 * i] = og ? e1 : e0;
+          o8[2 * i + 1] = og ? e3 : e2;
+        }
+        const int od = 16 * g + (hi ? 8 : 0);
+        const float lsum = og ? l1 : l0;
+        const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
+        const float inv = 1.f / lsum;
+        const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
+        const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
+        const bool lse_lane = (lane & ~2) == 0;  // lanes 0 (head 0) and 2 (head 1)
+        if (a.mode == kFixed && a.num_splits > 1) {
+          const int PS = a.num_splits;
+          store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
+          if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
+        } else if (complete && a.rows.o) {
+          const size_t r = row * a.rows.stride + (parts > 1 ? cp.qt : a.rows.slot);
+          store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
+          if (lse_lane) a.rows.lse[r] = lse_own;
+        } else if (complete) {
+          store_out8(a.out + row * kHeadDim + od, o8, inv);
+          if (a.lse && lse_lane) a.lse[row] = lse_own;
+        } else {
+          const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
+          store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
+          if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
+        }
       }
-      float ls = l_lane;
+
+      if (idx + 1 < R1) advance(P, S, Hkv, cp);
+    }
+  } else {
+    constexpr int kRowB = 2 * kHeadDim;  // one bf16 token row, bytes
+    // ---- consumer -------------------------------------------------------------
+    // Lane (grp, c8) holds dims 16*c8..16*c8+15 of tokens 4*grp..4*grp+3 for
+    // both query heads; fp32 pairs go through the packed (f32x2) FMA pipe.
+    TilePos cp = locate(P, S, Hkv, R0);
+    float2 q2[kG][8];    // scaled q, dims (16*c8 + 2j, +1)
+    float2 acc[kG][8];   // output accumulator, same dims
+    float m0 = neg_inf(), m1 = neg_inf(), l_lane = 0.f;
+    int piece_b0 = 0;
+    bool piece_first = true;
+
+    int k = 0;
+    for (int idx = R0; idx < R1; ++idx, ++k) {
+      const int stage = k % NSTAGE;
+      const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
+      if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
+        // a copy never landed: give the remaining ones a bounded wait, then stop
+        for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
+          mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
+        late_exit();
+        return;
+      }
+      unsigned char* st = wbuf + stage * kStageBytes;
+      const bool first = (idx == R0) || (cp.b == 0);
+      if (first) {
 #pragma unroll
-      for (int o = 2; o < 32; o <<= 1) ls += __shfl_xor_sync(kFull, ls, o);
-      const float lo = __shfl_xor_sync(kFull, ls, 1);
-      const float l0 = hsel ? lo : ls, l1 = hsel ? ls : lo;
-      const int og = b4 ? 1 : 0;             // output head of this lane
-      const int od = c8 * 16 + (b3 ? 8 : 0);  // output dims od .. od+7
-      const float lsum = og ? l1 : l0;
-      const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
-      const float inv = 1.f / lsum;
-      const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
-      const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
-      const bool lse_lane = (lane & 15) == 0;
-      if (a.mode == kFixed && a.num_splits > 1) {
-        const int PS = a.num_splits;
-        store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
-        if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
-      } else if (complete && a.rows.o) {
-        const size_t r = row * a.rows.stride + (parts > 1 ? cp.qt : a.rows.slot);
-        store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
-        if (lse_lane) a.rows.lse[r] = lse_own;
-      } else if (complete) {
-        store_out8(a.out + row * kHeadDim + od, o8, inv);
-        if (a.lse && lse_lane) a.lse[row] = lse_own;
-      } else {
-        const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
-        store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
-        if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
+        for (int g = 0; g < kG; ++g) {
+          const uint4* qs = reinterpret_cast<const uint4*>(st + F::kQOff + g * 256 + c8 * 32);
+          const uint4 qa = qs[0], qb = qs[1];
+          const uint32_t wq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            q2[g][j] = make_float2(bf_lo(wq[j]) * a.scale_log2, bf_hi(wq[j]) * a.scale_log2);
+            acc[g][j] = make_float2(0.f, 0.f);
+          }
+        }
+        m0 = neg_inf();
+        m1 = neg_inf();
+        l_lane = 0.f;
+        piece_b0 = cp.b;
+        piece_first = (idx == R0);
       }
+      const int nvalid = min(kBlock, P.ctx[cp.s] - abs_block(cp) * kBlock);
+
+      // ---- scores: 4 tokens x 2 heads of partial dots per lane ----------------
+      float sc[8];
+      const unsigned char* Ks = st + grp * 4 * kRowB + c8 * (kRowB / 8);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float2 kf[8];
+        load_row16(Ks + i * kRowB, kf);
+        float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          d0 = __ffma2_rn(q2[0][j], kf[j], d0);
+          d1 = __ffma2_rn(q2[1][j], kf[j], d1);
+        }
+        sc[2 * i] = d0.x + d0.y;
+        sc[2 * i + 1] = d1.x + d1.y;
+      }
+      // reduce-scatter over the 8 lanes of this group: value v = 2*i + g ends in
+      // the lane with (lane & 7) == v
+#pragma unroll
+      for (int step = 0; step < 3; ++step) {
+        const int half = 4 >> step;
+        const bool upper = (lane & half) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+          const float send = upper ? sc[j] : sc[j + half];
+          const float keep = upper ? sc[j + half] : sc[j];
+          sc[j] = keep + __shfl_xor_sync(kFull, send, half);
+        }
+      }
+      const int tok = grp * 4 + ((lane & 7) >> 1);
+      const float s_val = tok < nvalid ? sc[0] : neg_inf();
+
+      // ---- online softmax (log2 domain) ------------------------------------------
+      float mx = s_val;
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      const float mx_other = __shfl_xor_sync(kFull, mx, 1);
+      const float mn0 = fmaxf(m0, hsel ? mx_other : mx);
+      const float mn1 = fmaxf(m1, hsel ? mx : mx_other);
+      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p = ex2(s_val - (hsel ? mn1 : mn0));
+      l_lane = l_lane * (hsel ? al1 : al0) + p;
+      float* pbuf = reinterpret_cast<float*>(wbuf + L::kPOff);
+      pbuf[lane] = p;  // index 2*token + head
+      __syncwarp();
+      float pv[8];
+      {
+        const float4* pb = reinterpret_cast<const float4*>(pbuf + grp * 8);
+        const float4 p0 = pb[0], p1 = pb[1];
+        pv[0] = p0.x; pv[1] = p0.y; pv[2] = p0.z; pv[3] = p0.w;
+        pv[4] = p1.x; pv[5] = p1.y; pv[6] = p1.z; pv[7] = p1.w;
+      }
+      if (al0 != 1.f || al1 != 1.f) {
+        const float2 a0 = make_float2(al0, al0), a1 = make_float2(al1, al1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc[0][j] = __fmul2_rn(acc[0][j], a0);
+          acc[1][j] = __fmul2_rn(acc[1][j], a1);
+        }
+      }
+      // ---- PV ----------------------------------------------------------------------
+      const unsigned char* Vs = st + F::kTile + grp * 4 * kRowB + c8 * (kRowB / 8);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (nvalid == kBlock || grp * 4 + i < nvalid) {
+          // tokens past the context may hold anything (even NaN): skip, never 0*x
+          float2 vf[8];
+          load_row16(Vs + i * kRowB, vf);
+          const float2 p0 = make_float2(pv[2 * i], pv[2 * i]);
+          const float2 p1 = make_float2(pv[2 * i + 1], pv[2 * i + 1]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            acc[0][j] = __ffma2_rn(p0, vf[j], acc[0][j]);
+            acc[1][j] = __ffma2_rn(p1, vf[j], acc[1][j]);
+          }
+        }
+      }
+      __syncwarp();  // all lanes are done with this stage's K/V and with pbuf
+      // refill the stage now: finishing a piece below needs no stage memory, so
+      // its work overlaps the copy
+      if (pidx < R1) issue(stage);
+
+      const bool last = (idx == R1 - 1) || (cp.b == cp.nt - 1);
+      if (last) {
+        // ---- finish the piece: sum the 4 token groups' accumulators (lanes
+        // c8, c8+8, c8+16, c8+24) by a reduce-scatter over lane bits 4 and 3;
+        // lane (b4, b3, c8) ends with head b4, dims 16*c8 + 8*b3 .. +7 ----------
+        const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+        float h16[16];  // after lane bit 4: head b4, dims 16*c8 .. 16*c8+15
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 mine = b4 ? acc[1][j] : acc[0][j];
+          const float2 send = b4 ? acc[0][j] : acc[1][j];
+          h16[2 * j] = mine.x + __shfl_xor_sync(kFull, send.x, 16);
+          h16[2 * j + 1] = mine.y + __shfl_xor_sync(kFull, send.y, 16);
+        }
+        float o8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float mine = b3 ? h16[8 + i] : h16[i];
+          const float send = b3 ? h16[i] : h16[8 + i];
+          o8[i] = mine + __shfl_xor_sync(kFull, send, 8);
+        }
+        float ls = l_lane;
+#pragma unroll
+        for (int o = 2; o < 32; o <<= 1) ls += __shfl_xor_sync(kFull, ls, o);
+        const float lo = __shfl_xor_sync(kFull, ls, 1);
+        const float l0 = hsel ? lo : ls, l1 = hsel ? ls : lo;
+        const int og = b4 ? 1 : 0;             // output head of this lane
+        const int od = c8 * 16 + (b3 ? 8 : 0);  // output dims od .. od+7
+        const float lsum = og ? l1 : l0;
+        const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
+        const float inv = 1.f / lsum;
+        const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
+        const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
+        const bool lse_lane = (lane & 15) == 0;
+        if (a.mode == kFixed && a.num_splits > 1) {
+          const int PS = a.num_splits;
+          store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
+          if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
+        } else if (complete && a.rows.o) {
+          const size_t r = row * a.rows.stride + (parts > 1 ? cp.qt : a.rows.slot);
+          store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
+          if (lse_lane) a.rows.lse[r] = lse_own;
+        } else if (complete) {
+          store_out8(a.out + row * kHeadDim + od, o8, inv);
+          if (a.lse && lse_lane) a.lse[row] = lse_own;
+        } else {
+          const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
+          store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
+          if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
+        }
+      }
+
+      if (idx + 1 < R1) advance(P, S, Hkv, cp);
     }
 
-    if (idx + 1 < R1) advance(P, S, Hkv, cp);
   }
-
   late_exit();
 }
 
@@ -880,12 +1094,14 @@ constexpr int kWarps = 6;
 // (engine, ragged) run best with 6 warps x 2 CTAs per SM.
 constexpr int kWarpsLong = 8;
 constexpr int kStages = 2;    // bf16: 2 x 8 KB of copies in flight per warp
-// int8: 6 warps x 2 stages of 4.6 KB (a K and a V tile, each one copy of
-// codes and scales), two CTAs per SM. The int8 loop is bound by instruction
-// issue (the dequantising conversions), not by copies in flight: a sweep of
-// 4-8 warps x 2-3 stages put this shape level with the best on every batch.
-// FP8 pools share the int8 tile and shape.
-constexpr int kWarpsQ8 = 6;
+// 8-bit pools (int8, FP8): 8 warps x 2 stages of 4.7 KB (a K and a V tile,
+// each one copy of codes and scales), two CTAs per SM. Resident warps pay
+// more than stages: 16 per SM measured 6-11% faster than 12 (6 x 2) on the
+// ragged and long batches, while 7 x 3, 6 x 3 and 5 x 4 stages were 4-25%
+// slower; 3 CTAs of 6 warps need under 113 registers and spill. With the
+// per-tile math taken out, the 8 x 32k batch still takes 97% of its time:
+// there the 2112-byte copies, not the MMA loop, set the pace.
+constexpr int kWarpsQ8 = 8;
 constexpr int kStagesQ8 = 2;
 
 struct DecodeGeometry;
