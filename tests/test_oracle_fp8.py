@@ -64,6 +64,16 @@ def test_saturation_and_round_trip():
     assert np.array_equal(back, finite)
 
 
+def test_representable_row_is_exact():
+    # amax 448 -> inv 1 and scale 1: every finite E4M3 value comes back as its own code
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = oracle.e4m3_values(finite)
+    row = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16)
+    codes, scales = oracle.quantize_rows_f8(row.unsqueeze(0))
+    assert scales[0] == 1.0
+    assert np.array_equal(oracle.e4m3_values(codes[0]), vals)
+
+
 def _random_rows(seed, n=64, d=128):
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(n, d, generator=g)
@@ -84,7 +94,12 @@ def test_row_round_trip_within_half_a_step(seed):
     y = xf / s
     assert np.all(np.abs(xf - deq) <= (np.maximum(np.abs(y) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-5)) * s)
     amax_idx = np.abs(xf).argmax(axis=1)
-    assert np.all(oracle.e4m3_values(codes[np.arange(len(xf)), amax_idx]) ** 2 == 448.0 ** 2)
+    top = oracle.e4m3_values(codes[np.arange(len(xf)), amax_idx])
+    assert np.all(top ** 2 == 448.0 ** 2)
+    # and the largest element dequantises back to itself (the scale is the
+    # row's amax over 448, rounded once to fp32)
+    xtop = xf[np.arange(len(xf)), amax_idx]
+    assert np.all(np.abs(top * s[:, 0] - xtop) <= 2.0 ** -23 * np.abs(xtop))
 
 
 def test_zero_row_and_sign_symmetry():
