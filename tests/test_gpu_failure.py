@@ -47,6 +47,28 @@ def test_missing_copy_runs_into_the_bounded_wait():
     _still_usable(db)
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_missing_copy_in_the_8bit_loop_runs_into_the_bounded_wait(fmt):
+    from tests.gpu_util import Int8Batch
+    from tests.pools import oracle_attention_f8, oracle_attention_i8
+    w = W.tiny(seed=42)
+    db = Int8Batch(w, fp8=fmt == "fp8")
+    B.pa_debug_read_error()
+    B.pa_debug_inject_missing_copy(0)
+    t0 = time.time()
+    db.decode(0)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    err = B.pa_debug_read_error()
+    assert err & B.PA_DEVERR_PIPE_TIMEOUT, err
+    assert dt < 30, dt
+    out, lse = db.decode(0)
+    torch.cuda.synchronize()
+    assert B.pa_debug_read_error() == 0
+    ref, ref_lse = oracle_attention_f8(w) if fmt == "fp8" else oracle_attention_i8(w)
+    assert_attention_close(out, lse, ref, ref_lse, what=f"{fmt} call after the injected failure")
+
+
 def test_injection_is_consumed_by_one_launch():
     w = W.tiny(seed=41)
     db = DeviceBatch(w)
@@ -91,13 +113,16 @@ def test_window_longer_than_context_is_flagged():
     assert B.pa_debug_read_error() & B.PA_DEVERR_QLEN_RANGE
 
 
-def test_int8_bad_slot_and_block_are_flagged():
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_8bit_bad_slot_and_block_are_flagged(fmt):
     w = W.tiny(seed=44)
     dev = torch.device("cuda:0")
-    kc, vc = w.empty_pool_i8(dev)
+    fp8 = fmt == "fp8"
+    kc, vc = w.empty_pool_f8(dev) if fp8 else w.empty_pool_i8(dev)
     slots = w.slot_new.clone()
     slots[1] = w.num_blocks * w.block_size + 5
-    B.pa_reshape_and_cache_int8(w.k_new.to(dev), w.v_new.to(dev), slots.to(dev), kc, vc)
+    write = B.pa_reshape_and_cache_fp8 if fp8 else B.pa_reshape_and_cache_int8
+    write(w.k_new.to(dev), w.v_new.to(dev), slots.to(dev), kc, vc)
     torch.cuda.synchronize()
     assert B.pa_debug_read_error() & B.PA_DEVERR_SLOT_RANGE
     q = w.q.to(dev)
@@ -106,7 +131,12 @@ def test_int8_bad_slot_and_block_are_flagged():
     bt = bt.to(dev)
     out = torch.empty_like(q)
     sh = B.shape_of(q, kc, bt)
-    ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
-    B.pa_decode_int8(q, kc, vc, bt, w.context_lens.to(dev), w.scale, out, None, workspace=ws)
+    if fp8:
+        ws = B.workspace(B.pa_decode_fp8_workspace_size(sh, 0), dev)
+        B.pa_decode_fp8(q, kc, vc, bt, w.context_lens.to(dev), w.scale, out, None, workspace=ws)
+    else:
+        ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
+        B.pa_decode_int8(q, kc, vc, bt, w.context_lens.to(dev), w.scale, out, None,
+                         workspace=ws)
     torch.cuda.synchronize()
     assert B.pa_debug_read_error() & B.PA_DEVERR_BLOCK_RANGE

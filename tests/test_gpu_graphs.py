@@ -100,24 +100,28 @@ def test_varlen_graph_replay():
     assert_attention_close(out, lse, ref, ref_lse, what="varlen graph")
 
 
-def test_int8_write_and_decode_graph_replay():
-    # quantising cache write + int8 decode captured once; replayed after the
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_8bit_write_and_decode_graph_replay(fmt):
+    # quantising cache write + 8-bit decode captured once; replayed after the
     # new rows and the queries change in place
     w = W.engine(seed=63, num_seqs=24, context=300)
     dev = torch.device("cuda:0")
-    kc, vc = w.empty_pool_i8(dev)
-    B.pa_reshape_and_cache_int8(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev),
-                                kc, vc)
+    fp8 = fmt == "fp8"
+    write = B.pa_reshape_and_cache_fp8 if fp8 else B.pa_reshape_and_cache_int8
+    decode = B.pa_decode_fp8 if fp8 else B.pa_decode_int8
+    ws_size = B.pa_decode_fp8_workspace_size if fp8 else B.pa_decode_int8_workspace_size
+    kc, vc = w.empty_pool_f8(dev) if fp8 else w.empty_pool_i8(dev)
+    write(w.k_hist.to(dev), w.v_hist.to(dev), w.slot_hist.to(dev), kc, vc)
     k_new, v_new, slots = w.k_new.to(dev), w.v_new.to(dev), w.slot_new.to(dev)
     q, bt, cl = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
     sh = B.shape_of(q, kc, bt)
-    ws = B.workspace(B.pa_decode_int8_workspace_size(sh, 0), dev)
+    ws = B.workspace(ws_size(sh, 0), dev)
 
     def step():
-        B.pa_reshape_and_cache_int8(k_new, v_new, slots, kc, vc)
-        B.pa_decode_int8(q, kc, vc, bt, cl, w.scale, out, lse, workspace=ws)
+        write(k_new, v_new, slots, kc, vc)
+        decode(q, kc, vc, bt, cl, w.scale, out, lse, workspace=ws)
 
     step()
     torch.cuda.synchronize()
@@ -135,9 +139,9 @@ def test_int8_write_and_decode_graph_replay():
     torch.cuda.synchronize()
     assert B.pa_debug_read_error() == 0
     w.k_new, w.v_new, w.q = k2, v2, q2
-    from tests.pools import oracle_attention_i8
-    ref, ref_lse = oracle_attention_i8(w)
-    assert_attention_close(out, lse, ref, ref_lse, what="int8 graph replay")
+    from tests.pools import oracle_attention_f8, oracle_attention_i8
+    ref, ref_lse = oracle_attention_f8(w) if fp8 else oracle_attention_i8(w)
+    assert_attention_close(out, lse, ref, ref_lse, what=f"{fmt} graph replay")
 
 
 def test_cascade_graph_replay():
