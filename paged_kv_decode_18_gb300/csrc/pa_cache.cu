@@ -4,9 +4,13 @@
 // "Build an LLM Inference Engine From Scratch": chunked prefill gives a
 // bit-identical cache).
 //
-// A byte copy: each thread moves one 16-byte chunk of K and the matching
-// chunk of V. Reads of k/v are fully coalesced; each (token, KV head) row
-// lands as one contiguous 256-byte run of the (block, KV head) tile.
+// bf16 pool: a byte copy -- each thread moves one 16-byte chunk of K and the
+// matching chunk of V. Reads of k/v are fully coalesced; each (token, KV
+// head) row lands as one contiguous 256-byte run of the (block, KV head)
+// tile. 8-bit pools (int8, FP8 E4M3; course README, curriculum rows "The
+// Machine" and "Memory & KV Cache": fp8, quantization): one warp quantises
+// one row with its own fp32 scale and writes 128 code bytes plus the scale
+// into the tile.
 #include "pa_device.cuh"
 #include "pa_host.h"
 

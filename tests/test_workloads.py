@@ -94,3 +94,22 @@ def test_page_kv_cache_size_figures():
 def test_random_unique_slots():
     s = W.random_unique_slots(100, 20, 16, seed=1)
     assert s.unique().numel() == 100 and int(s.max()) < 320 and s.dtype == torch.int64
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_8bit_empty_pool_tiles(fmt):
+    # 2112-byte tiles: 16 x 128 sentinel codes, then 16 NaN scales; packing
+    # and splitting the tile layout are inverse
+    w = W.tiny(seed=3)
+    kc, vc = w.empty_pool_f8() if fmt == "fp8" else w.empty_pool_i8()
+    NB, H = w.num_blocks, w.num_kv_heads
+    assert kc.shape == (NB, H, W.INT8_TILE_BYTES) == vc.shape and kc.dtype == torch.uint8
+    codes, scales = W.int8_pool_split(kc)
+    sentinel = W.POOL_SENTINEL_F8 if fmt == "fp8" else W.POOL_SENTINEL_CODE & 0xFF
+    assert torch.all(codes.view(torch.uint8) == sentinel)
+    assert torch.all(torch.isnan(scales))
+    g = torch.Generator().manual_seed(4)
+    c2 = torch.randint(-128, 128, codes.shape, generator=g, dtype=torch.int8)
+    s2 = torch.rand(scales.shape, generator=g)
+    back = W.int8_pool_split(W.int8_pool_pack(c2, s2))
+    assert torch.equal(back[0], c2) and torch.equal(back[1], s2)
