@@ -454,6 +454,42 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
 
   for (int i = 0; i < NSTAGE && pidx < R1; ++i) issue(i);
 
+  // Waits for the copies of the k-th tile of this warp's range. false: a copy
+  // never landed -- the remaining ones get a bounded wait and the warp stops.
+  auto stage_ready = [&](int k) -> bool {
+    if (mbar_wait_bounded(smem_addr(&bars[k % NSTAGE]), (uint32_t)(k / NSTAGE) & 1u)) return true;
+    for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
+      mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
+    late_exit();
+    return false;
+  };
+
+  // Writes one lane's 8 output dims (query head og of the tile's KV head,
+  // dims od .. od+7, times inv) of a finished piece and, from lse_lane, its
+  // log-sum-exp: the output row when the piece is a whole (sequence, KV head)
+  // segment, else a partial -- the fixed split's slot, the partition's row or
+  // the worker's slot -- for the merge.
+  auto store_piece = [&](const TilePos& t, int og, int od, const float (&o8)[8], float inv,
+                         float lse_own, bool lse_lane, bool complete, bool piece_first) {
+    const size_t row = (size_t)t.s * Hq + (size_t)t.h * kG + og;
+    if (a.mode == kFixed && a.num_splits > 1) {
+      const int PS = a.num_splits;
+      store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
+      if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
+    } else if (complete && a.rows.o) {
+      const size_t r = row * a.rows.stride + (parts > 1 ? t.qt : a.rows.slot);
+      store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
+      if (lse_lane) a.rows.lse[r] = lse_own;
+    } else if (complete) {
+      store_out8(a.out + row * kHeadDim + od, o8, inv);
+      if (a.lse && lse_lane) a.lse[row] = lse_own;
+    } else {
+      const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
+      store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
+      if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
+    }
+  };
+
   if constexpr (Q8) {
     // ---- consumer, 8-bit tiles: the two contractions of a tile on warp MMAs
     // (m16n8k16, f16 operands, fp32 accumulation). Lane (g, c) = (lane / 4,
@@ -483,14 +519,8 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
 
     int k = 0;
     for (int idx = R0; idx < R1; ++idx, ++k) {
+      if (!stage_ready(k)) return;
       const int stage = k % NSTAGE;
-      const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
-      if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
-        for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
-          mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
-        late_exit();
-        return;
-      }
       unsigned char* st = wbuf + stage * kStageBytes;
       const bool first = (idx == R0) || (cp.b == 0);
       if (first) {
@@ -665,24 +695,8 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
         const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
         const float inv = 1.f / lsum;
         const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
-        const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
         const bool lse_lane = (lane & ~2) == 0;  // lanes 0 (head 0) and 2 (head 1)
-        if (a.mode == kFixed && a.num_splits > 1) {
-          const int PS = a.num_splits;
-          store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
-          if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
-        } else if (complete && a.rows.o) {
-          const size_t r = row * a.rows.stride + (parts > 1 ? cp.qt : a.rows.slot);
-          store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
-          if (lse_lane) a.rows.lse[r] = lse_own;
-        } else if (complete) {
-          store_out8(a.out + row * kHeadDim + od, o8, inv);
-          if (a.lse && lse_lane) a.lse[row] = lse_own;
-        } else {
-          const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
-          store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
-          if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
-        }
+        store_piece(cp, og, od, o8, inv, lse_own, lse_lane, complete, piece_first);
       }
 
       if (idx + 1 < R1) advance(P, S, Hkv, cp);
@@ -701,15 +715,8 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
 
     int k = 0;
     for (int idx = R0; idx < R1; ++idx, ++k) {
+      if (!stage_ready(k)) return;
       const int stage = k % NSTAGE;
-      const uint32_t parity = (uint32_t)(k / NSTAGE) & 1u;
-      if (!mbar_wait_bounded(smem_addr(&bars[stage]), parity)) {
-        // a copy never landed: give the remaining ones a bounded wait, then stop
-        for (int j = k + 1; j < k + NSTAGE && R0 + j < pidx; ++j)
-          mbar_wait_bounded(smem_addr(&bars[j % NSTAGE]), (uint32_t)(j / NSTAGE) & 1u);
-        late_exit();
-        return;
-      }
       unsigned char* st = wbuf + stage * kStageBytes;
       const bool first = (idx == R0) || (cp.b == 0);
       if (first) {
@@ -848,29 +855,12 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
         const float lse_own = ((og ? m1 : m0) + lg2(lsum)) * kLn2;
         const float inv = 1.f / lsum;
         const bool complete = (piece_b0 == 0) && (cp.b == cp.nt - 1);
-        const size_t row = (size_t)cp.s * Hq + (size_t)cp.h * kG + og;
         const bool lse_lane = (lane & 15) == 0;
-        if (a.mode == kFixed && a.num_splits > 1) {
-          const int PS = a.num_splits;
-          store_f8(a.part_o + (row * PS + fixed_p) * kHeadDim + od, o8, inv);
-          if (lse_lane) a.part_lse[row * PS + fixed_p] = lse_own;
-        } else if (complete && a.rows.o) {
-          const size_t r = row * a.rows.stride + (parts > 1 ? cp.qt : a.rows.slot);
-          store_f8(a.rows.o + r * kHeadDim + od, o8, inv);
-          if (lse_lane) a.rows.lse[r] = lse_own;
-        } else if (complete) {
-          store_out8(a.out + row * kHeadDim + od, o8, inv);
-          if (a.lse && lse_lane) a.lse[row] = lse_own;
-        } else {
-          const size_t slot = (size_t)w * 2 + (piece_first ? 0 : 1);
-          store_f8(a.part_o + (slot * kG + og) * kHeadDim + od, o8, inv);
-          if (lse_lane) a.part_lse[slot * kG + og] = lse_own;
-        }
+        store_piece(cp, og, od, o8, inv, lse_own, lse_lane, complete, piece_first);
       }
 
       if (idx + 1 < R1) advance(P, S, Hkv, cp);
     }
-
   }
   late_exit();
 }
