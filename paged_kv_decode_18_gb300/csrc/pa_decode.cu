@@ -501,9 +501,9 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
     // the k index pairs (2c, 2c+1) and (2c+8, 2c+9) are dims 32c + 4j + 0..3,
     // so each lane reads 32 contiguous bytes of rows g and g + 8.
     // Output: A = the V codes transposed (rows = dims, k = tokens), B = the
-    // softmax weights times each row's V scale, divided by the tile's largest
-    // V scale vmax (so in [0, 1], f16), and the MMA result times vmax joins
-    // the fp32 accumulator. For MMA m, row g is dim 16g + 2m and row g + 8 is
+    // softmax weights times each row's V scale, divided by the largest such
+    // product of the head in the tile (so in [0, 1], f16), and the MMA result
+    // times that product joins the fp32 accumulator. For MMA m, row g is dim 16g + 2m and row g + 8 is
     // dim 16g + 2m + 1; k pairs (2c, 2c+1) and (2c+8, 2c+9) are tokens 4c ..
     // 4c+3, so each lane reads 16 contiguous bytes of four token rows.
     const int g = lane >> 2, c = lane & 3;
@@ -616,15 +616,23 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
       const float4 pw = *reinterpret_cast<const float4*>(pbuf + hq * 16 + 4 * c);
       const float4 vs4 =
           *reinterpret_cast<const float4*>(st + F::kTile + F::kScaleOff + 16 * c);
-      // rows past the context may hold anything: their scale counts as 0
-      const float v0 = 4 * c < nvalid ? vs4.x : 0.f, v1 = 4 * c + 1 < nvalid ? vs4.y : 0.f;
-      const float v2 = 4 * c + 2 < nvalid ? vs4.z : 0.f, v3 = 4 * c + 3 < nvalid ? vs4.w : 0.f;
-      float vmax = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
-      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 1));
-      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 2));
-      const float rv = vmax > 0.f ? 1.f / vmax : 0.f;
-      const uint32_t b0 = pack_h2(pw.x * (v0 * rv), pw.y * (v1 * rv));
-      const uint32_t b1 = pack_h2(pw.z * (v2 * rv), pw.w * (v3 * rv));
+      // weight x V scale of tokens 4c .. 4c+3 for head hq; rows past the
+      // context may hold anything: their scale counts as 0
+      const float x0 = pw.x * (4 * c < nvalid ? vs4.x : 0.f);
+      const float x1 = pw.y * (4 * c + 1 < nvalid ? vs4.y : 0.f);
+      const float x2 = pw.z * (4 * c + 2 < nvalid ? vs4.z : 0.f);
+      const float x3 = pw.w * (4 * c + 3 < nvalid ? vs4.w : 0.f);
+      // normalised by the head's largest in the tile: the weights that carry
+      // the result keep f16's full relative precision, whatever the spread of
+      // the rows' scales
+      float xm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      xm = fmaxf(xm, __shfl_xor_sync(kFull, xm, 1));
+      xm = fmaxf(xm, __shfl_xor_sync(kFull, xm, 2));
+      const float rx = xm > 0.f ? 1.f / xm : 0.f;
+      const float xm_o = __shfl_xor_sync(kFull, xm, 4);  // lane g ^ 1: the other head
+      const float xm0 = hq ? xm_o : xm, xm1 = hq ? xm : xm_o;
+      const uint32_t b0 = pack_h2(x0 * rx, x1 * rx);
+      const uint32_t b1 = pack_h2(x2 * rx, x3 * rx);
 
       // ---- output ------------------------------------------------------------------
       const unsigned char* Vt = st + F::kTile;
@@ -662,8 +670,10 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
         codes_to_h2<FMT>(x23, a2, a3);
         float dv[4] = {0.f, 0.f, 0.f, 0.f};
         mma_16816(dv, a0, a1, a2, a3, b0, b1);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[m][q] = fmaf(vmax, dv[q], acc[m][q]);
+        acc[m][0] = fmaf(xm0, dv[0], acc[m][0]);
+        acc[m][1] = fmaf(xm1, dv[1], acc[m][1]);
+        acc[m][2] = fmaf(xm0, dv[2], acc[m][2]);
+        acc[m][3] = fmaf(xm1, dv[3], acc[m][3]);
       }
       __syncwarp();  // all lanes are done with this stage and with pbuf
       if (pidx < R1) issue(stage);
