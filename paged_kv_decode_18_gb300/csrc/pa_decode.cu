@@ -503,9 +503,10 @@ __global__ void __launch_bounds__(NWARPS * 32, FMT != kFmtBf16 || NWARPS <= 6 ? 
     // Output: A = the V codes transposed (rows = dims, k = tokens), B = the
     // softmax weights times each row's V scale, divided by the largest such
     // product of the head in the tile (so in [0, 1], f16), and the MMA result
-    // times that product joins the fp32 accumulator. For MMA m, row g is dim 16g + 2m and row g + 8 is
-    // dim 16g + 2m + 1; k pairs (2c, 2c+1) and (2c+8, 2c+9) are tokens 4c ..
-    // 4c+3, so each lane reads 16 contiguous bytes of four token rows.
+    // times that product joins the fp32 accumulator. For MMA m, row g is dim
+    // 16g + 2m and row g + 8 is dim 16g + 2m + 1; k pairs (2c, 2c+1) and
+    // (2c+8, 2c+9) are tokens 4c .. 4c+3, so each lane reads 16 contiguous
+    // bytes of four token rows.
     const int g = lane >> 2, c = lane & 3;
     const int hq = g & 1;  // the head of B column g
     TilePos cp = locate(P, S, Hkv, R0);
