@@ -278,7 +278,11 @@ int pa_reshape_and_cache_int8(const pa_bf16* k, const pa_bf16* v, const int64_t*
  * int8 V row. Same arguments, splits, outputs and workspace rules as
  * pa_decode (workspace from pa_decode_int8_workspace_size); k_cache and
  * v_cache 16-byte aligned. The result is attention over the dequantised
- * rows, within fp32 rounding.
+ * rows: q and the codes enter the products exactly and all sums are fp32;
+ * each softmax weight times its row's V scale is rounded to f16 relative to
+ * the largest such product of its head in the 16-token block (relative error
+ * 2^-11, as when P is rounded to 16 bits); the log-sum-exp comes from fp32
+ * sums.
  */
 int pa_decode_int8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
                    const int32_t* block_tables, const int32_t* context_lens, float scale,
@@ -321,7 +325,8 @@ int pa_reshape_and_cache_fp8(const pa_bf16* k, const pa_bf16* v, const int64_t* 
  * result (they may hold anything, NaN codes included). Same arguments,
  * splits, outputs and workspace rules as pa_decode (workspace from
  * pa_decode_fp8_workspace_size); k_cache and v_cache 16-byte aligned. The
- * result is attention over the dequantised rows, within fp32 rounding.
+ * result is attention over the dequantised rows, with the precision stated
+ * for pa_decode_int8.
  */
 int pa_decode_fp8(const pa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens, float scale,
